@@ -1,0 +1,40 @@
+"""Compile the fp64 CPU oracle (``finalize_ref.c``) into a shared library.
+
+TEST INFRASTRUCTURE ONLY: the library is loaded by the test suite, the smoke
+check and the benchmark's CPU-baseline leg, never by the CUDA path.
+
+Contraction of multiply-adds is switched off so that the oracle gives the
+same doubles on x86-64 and on AArch64.
+"""
+import os
+import subprocess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "finalize_ref.c")
+OUT_DIR = os.path.join(HERE, "_build")
+LIB = os.path.join(OUT_DIR, "liboracle.so")
+
+
+_FLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+          "-shared", "-fPIC", "-Wall", "-Wextra"]
+
+
+def compile_source(src_path: str, lib_path: str) -> str:
+    """Compile one C source with the oracle's flags into ``lib_path``."""
+    tmp = lib_path + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *_FLAGS, "-o", tmp, src_path, "-lm"], check=True)
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build_oracle(force: bool = False) -> str:
+    """Build ``_build/liboracle.so`` if it is missing or older than its source."""
+    if (not force and os.path.exists(LIB)
+            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
+        return LIB
+    os.makedirs(OUT_DIR, exist_ok=True)
+    return compile_source(SRC, LIB)
+
+
+if __name__ == "__main__":
+    print(build_oracle(force=True))

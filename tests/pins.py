@@ -1,0 +1,283 @@
+"""Checks that pin the fp64 oracle to facts other than itself.
+
+Each ``pin_*`` takes an oracle object (the real one, or a copy built from a
+deliberately broken source by the mutation test) and raises AssertionError
+when the oracle disagrees with:
+
+  * values worked out by hand (``tests/golden``);
+  * special cases with an exact answer (one slot of weight 1, zero weights,
+    zero routed scale, a constant row under RMSNorm);
+  * invariants (slot order, linearity, padding never read, equal tokens);
+  * library routines (torch's bf16 conversion and RMSNorm).
+
+The operation is the deferred finalize of "Support deferred MoE finalize for
+MXFP4 and FP8 block-scale" (Motivation; Modifications item 2), with the
+residual and RMSNorm of "[Kimi K2.5] Fuse deferred MoE finalize into
+next-layer AR + residual + RMSNorm" (Summary) and the packed routing words of
+"[Deepseek V4] Keep fp32 routing weights in the mxfp4 trtllm MoE".
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from moe_deferred_finalize_gb300.workloads import bf16_bits_to_f32, synth, to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _bits(x):
+    return to_bf16_bits(np.asarray(x, np.float64))
+
+
+def _rand_problem(seed, T=5, K=3, H=40, P=None, with_norm=False):
+    rng = np.random.default_rng(seed)
+    P = P or (T * K + 7)
+    x = _bits(rng.standard_normal((P, H)))
+    idx = np.stack([rng.choice(P, K, replace=False) for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, K)).astype(np.float32)
+    shared = _bits(rng.standard_normal((T, H)))
+    res = _bits(2 * rng.standard_normal((T, H))) if with_norm else None
+    gamma = _bits(rng.uniform(0.5, 1.5, H)) if with_norm else None
+    return x, idx, w, shared, res, gamma
+
+
+# ------------------------------------------------------------ finalize pins
+
+
+def pin_golden_hand_worked(orc):
+    g = _load("hand_worked_t2_k2_h3.json")
+    x = _bits(g["permuted_out"])
+    idx = np.array(g["idx"], np.int32)
+    shared = _bits(g["shared"])
+    res = _bits(g["residual"])
+    gamma = _bits(g["gamma"])
+    weights = {
+        "fp32": np.array(g["weights_fp32"], np.float32),
+        "bf16": np.array(g["weights_bf16_bits"], np.uint16),
+        "packed": np.array(g["weights_packed"], np.int64).astype(np.int32).reshape(2, 2),
+    }
+    want_norm = np.array([[float(Fraction(v)) for v in row] for row in g["norm_out"]])
+    for kind, w in weights.items():
+        r = orc.moe_finalize(x, idx, w, kind, g["routed_scale"], shared, res, gamma, g["eps"])
+        assert np.array_equal(r["out"], np.array(g["out"], np.float64)), (kind, r["out"])
+        assert np.array_equal(r["residual_out"], np.array(g["residual_out"], np.float64)), kind
+        assert np.allclose(r["norm_out"], want_norm, rtol=1e-15, atol=0), (kind, r["norm_out"])
+        r2 = orc.moe_finalize(x, idx, w, kind, g["routed_scale"], shared)
+        assert np.array_equal(r2["out"], np.array(g["out"], np.float64)), kind
+
+
+def pin_k1_identity(orc):
+    """K=1, weight 1, scale 1, zero shared: out is the gathered row, exactly."""
+    x, idx, _, shared, _, _ = _rand_problem(1, T=7, K=1, H=33)
+    w = np.ones((7, 1), np.float32)
+    zero = np.zeros_like(shared)
+    r = orc.moe_finalize(x, idx, w, "fp32", 1.0, zero)
+    assert np.array_equal(r["out"], bf16_bits_to_f32(x[idx[:, 0]]).astype(np.float64))
+
+
+def pin_zero_weights(orc):
+    """All routing weights 0: out is the shared-expert output, exactly."""
+    x, idx, _, shared, _, _ = _rand_problem(2)
+    w = np.zeros(idx.shape, np.float32)
+    r = orc.moe_finalize(x, idx, w, "fp32", 2.5, shared)
+    assert np.array_equal(r["out"], bf16_bits_to_f32(shared).astype(np.float64))
+
+
+def pin_zero_scale(orc):
+    """Routed scale 0 with nonzero weights: out is the shared output, exactly."""
+    x, idx, w, shared, _, _ = _rand_problem(3)
+    r = orc.moe_finalize(x, idx, w, "fp32", 0.0, shared)
+    assert np.array_equal(r["out"], bf16_bits_to_f32(shared).astype(np.float64))
+
+
+def pin_slot_permutation(orc):
+    """Reordering the k slots (row and weight together) changes nothing."""
+    x, idx, w, shared, res, gamma = _rand_problem(4, K=6, with_norm=True)
+    a = orc.moe_finalize(x, idx, w, "fp32", 2.5, shared, res, gamma, 1e-6)
+    perm = np.random.default_rng(5).permutation(6)
+    b = orc.moe_finalize(x, idx[:, perm], w[:, perm], "fp32", 2.5, shared, res, gamma, 1e-6)
+    for key in a:
+        assert np.allclose(a[key], b[key], rtol=1e-13, atol=1e-13), key
+
+
+def pin_linearity(orc):
+    """out - shared scales with the routed scale; out moves one-for-one with shared."""
+    x, idx, w, shared, _, _ = _rand_problem(6)
+    sh = bf16_bits_to_f32(shared).astype(np.float64)
+    r1 = orc.moe_finalize(x, idx, w, "fp32", 1.0, shared)["out"] - sh
+    r3 = orc.moe_finalize(x, idx, w, "fp32", 3.0, shared)["out"] - sh
+    assert np.allclose(r3, 3.0 * r1, rtol=1e-13, atol=1e-12)
+    assert np.abs(r1).max() > 0.1
+    zero = np.zeros_like(shared)
+    r0 = orc.moe_finalize(x, idx, w, "fp32", 1.0, zero)["out"]
+    assert np.allclose(r0 + sh, r1 + sh, rtol=1e-13, atol=1e-12)
+    assert np.allclose(orc.moe_finalize(x, idx, w, "fp32", 1.0, shared)["out"], r0 + sh,
+                       rtol=1e-13, atol=1e-12)
+
+
+def pin_padding_never_read(orc):
+    """NaN in every padding row leaves every output finite."""
+    wl = synth("pad", T=24, K=4, H=48, E=64, tile=16, P=128, weight_rule="sigmoid",
+               routed_scale=2.5, with_norm=True, seed=7)
+    x = wl.permuted_out.copy()
+    x[~wl.valid_rows] = 0x7FC0          # bf16 quiet NaN
+    r = orc.moe_finalize(x, wl.idx, wl.weights, "fp32", wl.routed_scale, wl.shared,
+                         wl.residual, wl.gamma, wl.eps)
+    for key, v in r.items():
+        assert np.isfinite(v).all(), key
+
+
+def pin_duplicate_tokens(orc):
+    """Two tokens with identical inputs give identical rows."""
+    x, idx, w, shared, res, gamma = _rand_problem(8, T=4, with_norm=True)
+    idx[2], w[2], shared[2], res[2] = idx[0], w[0], shared[0], res[0]
+    r = orc.moe_finalize(x, idx, w, "fp32", 1.5, shared, res, gamma, 1e-6)
+    for key, v in r.items():
+        assert np.array_equal(v[0], v[2]), key
+        assert not np.array_equal(v[0], v[1]), key
+
+
+def pin_residual_add(orc):
+    """residual_out - out is the residual, to fp64 rounding."""
+    x, idx, w, shared, res, gamma = _rand_problem(9, with_norm=True)
+    r = orc.moe_finalize(x, idx, w, "fp32", 2.5, shared, res, gamma, 1e-6)
+    assert np.allclose(r["residual_out"] - r["out"], bf16_bits_to_f32(res), rtol=0, atol=1e-12)
+
+
+def pin_bad_index(orc):
+    x, idx, w, shared, _, _ = _rand_problem(10)
+    for bad in (-1, x.shape[0]):
+        j = idx.copy()
+        j[1, 1] = bad
+        try:
+            orc.moe_finalize(x, j, w, "fp32", 1.0, shared)
+        except ValueError:
+            continue
+        raise AssertionError(f"index {bad} accepted")
+
+
+# ------------------------------------------------------------- RMSNorm pins
+
+
+def _norm_only(orc, s_bits, gamma_bits, eps):
+    """RMSNorm through the finalize: K=1 slot of weight 0, shared 0, residual s."""
+    T, H = s_bits.shape
+    x = np.zeros((1, H), np.uint16)
+    idx = np.zeros((T, 1), np.int32)
+    w = np.zeros((T, 1), np.float32)
+    zero = np.zeros((T, H), np.uint16)
+    return orc.moe_finalize(x, idx, w, "fp32", 1.0, zero, s_bits, gamma_bits, eps)["norm_out"]
+
+
+def pin_rmsnorm_constant_row(orc):
+    """A constant row c gives c / sqrt(c^2 + eps) * gamma."""
+    H = 37
+    gamma = _bits(np.linspace(0.5, 1.5, H))
+    g = bf16_bits_to_f32(gamma).astype(np.float64)
+    for c, eps in ((3.0, 1e-6), (-0.125, 1e-2), (1.0, 0.0)):
+        s = _bits(np.full((2, H), c))
+        y = _norm_only(orc, s, gamma, eps)
+        want = c / math.sqrt(c * c + eps) * g
+        assert np.allclose(y, want[None, :], rtol=1e-14, atol=0), (c, eps)
+
+
+def pin_rmsnorm_unit_mean_square(orc):
+    """mean((norm_out / gamma)^2) = ms / (ms + eps) for any row."""
+    rng = np.random.default_rng(11)
+    T, H, eps = 3, 96, 0.5
+    s = _bits(2 * rng.standard_normal((T, H)))
+    gamma = _bits(rng.uniform(0.5, 1.5, H))
+    y = _norm_only(orc, s, gamma, eps)
+    sf = bf16_bits_to_f32(s).astype(np.float64)
+    ms = (sf * sf).mean(axis=1)
+    got = ((y / bf16_bits_to_f32(gamma)) ** 2).mean(axis=1)
+    assert np.allclose(got, ms / (ms + eps), rtol=1e-13)
+
+
+def pin_rmsnorm_library(orc):
+    """Agrees with torch's RMSNorm in float64 (mean over H, eps inside the root)."""
+    rng = np.random.default_rng(12)
+    T, H, eps = 4, 130, 1e-6
+    s = _bits(2 * rng.standard_normal((T, H)))
+    gamma = _bits(rng.uniform(0.5, 1.5, H))
+    y = _norm_only(orc, s, gamma, eps)
+    ref = torch.nn.functional.rms_norm(
+        torch.from_numpy(bf16_bits_to_f32(s).astype(np.float64)), (H,),
+        weight=torch.from_numpy(bf16_bits_to_f32(gamma).astype(np.float64)), eps=eps).numpy()
+    assert np.allclose(y, ref, rtol=1e-13, atol=0)
+    y2 = orc.rmsnorm_bf16(s, gamma, eps)
+    assert np.allclose(y2, ref, rtol=1e-13, atol=0)
+
+
+# -------------------------------------------------------- pack/unpack pins
+
+
+def _u32(h):
+    return np.array([int(h, 16)], np.uint64).astype(np.uint32).view(np.int32)[0]
+
+
+def pin_unpack_golden(orc):
+    g = _load("packed_topk_ids.json")
+    words = np.array([_u32(e["word_hex"]) for e in g["unpack"]], np.int32)
+    ex, w = orc.unpack_topk_ids(words)
+    for i, e in enumerate(g["unpack"]):
+        assert ex[i] == e["expert"], e
+        want = {"inf": math.inf, "-0": -0.0, "2^-133": 2.0 ** -133}.get(e["weight"], e["weight"])
+        assert w[i] == want and math.copysign(1, w[i]) == math.copysign(1, want), (e, w[i])
+
+
+def pin_pack_golden(orc):
+    g = _load("packed_topk_ids.json")
+    for e in g["pack"]:
+        f = np.array([_u32(e["weight_f32_hex"])], np.int32).view(np.float32)[0]
+        assert orc.pack_topk_id(e["expert"], f) == _u32(e["word_hex"]), e
+
+
+def pin_unpack_exhaustive(orc):
+    """Every low half, against torch's bf16 -> fp32 widening; expert ids as
+    unsigned high halves; pack(unpack(x)) == x except for signalling NaNs."""
+    low = np.arange(65536, dtype=np.uint32)
+    hi = np.array([0, 1, 255, 383, 32767, 32768, 65535], np.uint32)
+    words = ((hi[:, None] << 16) | low[None, :]).ravel().view(np.int32)
+    ex, w = orc.unpack_topk_ids(words)
+    ref = torch.from_numpy(low.astype(np.uint16).view(np.int16)).view(torch.bfloat16).float().numpy()
+    ref = np.tile(ref, hi.size)
+    assert np.array_equal(ex, np.repeat(hi, 65536).astype(np.int32))
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(w), nan)
+    assert np.array_equal(w[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+    # round trip on one high half (the C packer is called per value)
+    sel = np.arange(0, 65536, 7)
+    for i in sel:
+        if nan[i]:
+            continue
+        assert orc.pack_topk_id(int(ex[i]), float(w[i])) == words[i], hex(int(words[i]))
+
+
+def pin_bf16_rounding_library(orc):
+    """fp32 -> bf16 agrees with torch's conversion (round to nearest even)."""
+    rng = np.random.default_rng(13)
+    u = rng.integers(0, 2**32, 20000, dtype=np.uint64).astype(np.uint32)
+    ties = (rng.integers(0, 2**16, 3000, dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    special = np.array([0x00000000, 0x80000000, 0x7F800000, 0xFF800000, 0x7F7FFFFF,
+                        0x00008000, 0x00018000, 0x3F808000, 0x3F818000, 0x7F7F8000],
+                       np.uint32)
+    f = np.concatenate([u, ties, special]).view(np.float32)
+    f = f[~np.isnan(f)]
+    mine = orc.f32_to_bf16(f)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(mine, ref)
+    qnan = orc.f32_to_bf16(np.array([0x7F800001, 0xFFC00000], np.uint32).view(np.float32))
+    assert np.isnan(bf16_bits_to_f32(qnan)).all() and ((qnan & 0x0040) != 0).all()
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,72 @@
+"""Plants plausible mistakes in copies of the oracle's C source and checks
+that the pins catch every one of them.  CPU only; the real oracle source is
+never modified."""
+import os
+
+import pytest
+
+import oracle
+from oracle.build import SRC, compile_source
+
+import pins
+
+# (name, text in finalize_ref.c, replacement)
+MUTANTS = [
+    ("drop_shared", "m += bf16_to_double(shared[t * H + h]);", ""),
+    ("shared_sign", "m += bf16_to_double(shared[t * H + h]);",
+     "m -= bf16_to_double(shared[t * H + h]);"),
+    ("drop_routed_scale", "double w = routed_scale * decode_weight(",
+     "double w = decode_weight("),
+    ("scale_added", "double w = routed_scale * decode_weight(weights, wkind, t * K + k);",
+     "double w = routed_scale + decode_weight(weights, wkind, t * K + k);"),
+    ("idx_transposed", "permuted_out + (int64_t)idx[t * K + k] * H",
+     "permuted_out + (int64_t)idx[k * T + t] * H"),
+    ("weight_slot_shift", "decode_weight(weights, wkind, t * K + k)",
+     "decode_weight(weights, wkind, t * K + (k + 1) % K)"),
+    ("drop_last_slot", "for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 0; k < K - 1; ++k) {"),
+    ("drop_residual", "m + bf16_to_double(residual[t * H + h])", "m"),
+    ("eps_outside_root", "1.0 / sqrt(sum_sq / (double)H + eps)",
+     "1.0 / (sqrt(sum_sq / (double)H) + eps)"),
+    ("mean_over_h_minus_1", "double inv_rms = 1.0 / sqrt(sum_sq / (double)H + eps);\n"
+     "        for (int64_t h = 0; h < H; ++h)\n            y[t * H + h] = row[h]",
+     "double inv_rms = 1.0 / sqrt(sum_sq / (double)(H - 1) + eps);\n"
+     "        for (int64_t h = 0; h < H; ++h)\n            y[t * H + h] = row[h]"),
+    ("drop_gamma", "y[t * H + h] = row[h] * inv_rms * bf16_to_double(gamma[h]);",
+     "y[t * H + h] = row[h] * inv_rms;"),
+    ("gamma_offset", "y[t * H + h] = row[h] * inv_rms * bf16_to_double(gamma[h]);",
+     "y[t * H + h] = row[h] * inv_rms * (1.0 + bf16_to_double(gamma[h]));"),
+    ("norm_of_out_not_residual", "rmsnorm_rows_double(residual_out, gamma",
+     "rmsnorm_rows_double(out, gamma"),
+    ("expert_id_signed_shift", "expert_ids[i] = (int32_t)(word >> 16);",
+     "expert_ids[i] = packed[i] >> 16;"),
+    ("weight_sign_dropped", "bits_to_float((word & 0xFFFFu) << 16)",
+     "bits_to_float((word & 0x7FFFu) << 16)"),
+    ("weight_from_high_half", "bits_to_float((word & 0xFFFFu) << 16)",
+     "bits_to_float(word & 0xFFFF0000u)"),
+    ("pack_truncates", "if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))",
+     "if (0)"),
+    ("pack_ties_away", "if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))",
+     "if (dropped >= 0x8000u)"),
+    ("bf16_weight_read_as_packed", "if (wkind == OREF_W_BF16)", "if (0)"),
+    ("bad_index_accepted", "if (idx[i] < 0 || (int64_t)idx[i] >= P) return -1;",
+     "if (idx[i] < 0) return -1;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new)
+    path = os.path.join(tmp_path, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(mutated)
+    lib = compile_source(path, os.path.join(tmp_path, f"lib{name}.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the mutant {name}"
