@@ -1,0 +1,474 @@
+"""Benchmark of the deferred MoE finalize (one JSON line on stdout).
+
+Headline: HBM GB/s of one finalize step at T=16384, K=8, H=7168 with
+residual add + RMSNorm (residual_out and norm_out emitted, out not written),
+inputs resident in HBM.  Algorithmic bytes per step = gathered rows
+(T*K*H*2) + shared and residual read + residual_out and norm_out written
+(4*T*H*2) + gamma (H*2) + idx and fp32 weights (T*K*8).
+
+Also reported on the same line:
+  * decode latency, microseconds per call at T=1 (packed routing) and
+    T=256 (fp32 routing), each call on inputs no earlier call touched
+    (rotating copies larger than L2), timed as CUDA-graph replays and as
+    back-to-back eager calls;
+  * roofline of the finalize kernel against the measured HBM copy peak;
+  * e2e: the same GB/s with host (pinned) inputs copied in and results
+    copied out inside the timed region;
+  * cpu_baseline: the fp64 CPU oracle on the host cores (test
+    infrastructure, timed only here);
+  * SM clocks and throttle reasons sampled during the timed region.
+
+``--impl reference`` times the fp64 CPU oracle on the same workload
+(bounded token samples per step) and prints the same line shape.
+
+Multi-GPU: every rank runs its own full-size problem (the finalize is
+token-local, no data exchange); the job value is the bytes of all ranks
+over the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_deferred_finalize_gb300 import workloads as W  # noqa: E402
+
+WORKLOAD = "prefill_t16384"
+METRIC = "finalize µs/call at T=1,256; HBM GB/s (% of peak) at T=16384, H=7168"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "moe_deferred_finalize_gb300", "csrc", "finalize.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def algorithmic_bytes(T, K, H, wbytes, norm, write_out):
+    """Bytes the finalize must move: every gathered valid row once, every
+    dense [T, H] operand once, gamma once, the row map and weights once."""
+    dense = 1 + (1 if write_out else 0) + (3 if norm else 0)   # shared, out, residual, r_out, n_out
+    return T * K * H * 2 + dense * T * H * 2 + (H * 2 if norm else 0) + T * K * (4 + wbytes)
+
+
+def workload_bytes(wl, write_out):
+    wbytes = {"fp32": 4, "bf16": 2, "packed": 4}[wl.wkind]
+    return algorithmic_bytes(wl.T, wl.K, wl.H, wbytes, wl.with_norm, write_out)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """ncu DRAM bytes per launch recorded for the current kernel source, else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    if d.get("kernel_src_sha256") != sha or d.get("workload") != WORKLOAD:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def pinned_alloc(shape, dtype):
+    tdt = {np.dtype(np.uint16): torch.int16, np.dtype(np.int32): torch.int32,
+           np.dtype(np.float32): torch.float32}[np.dtype(dtype)]
+    t = torch.empty(shape, dtype=tdt, pin_memory=True)
+    a = t.numpy()
+    return a.view(np.uint16) if np.dtype(dtype) == np.uint16 else a
+
+
+def host_tensor(a):
+    """torch view (no copy) of a numpy array; bf16 bits become bfloat16."""
+    t = torch.from_numpy(a)
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    return t
+
+
+# --------------------------------------------------------- GPU measurement
+
+
+def device_inputs(wl, device):
+    d = {"x": host_tensor(wl.permuted_out).to(device),
+         "idx": host_tensor(wl.idx).to(device),
+         "w": host_tensor(np.ascontiguousarray(wl.weights)).to(device),
+         "shared": host_tensor(wl.shared).to(device)}
+    if wl.with_norm:
+        d["residual"] = host_tensor(wl.residual).to(device)
+        d["gamma"] = host_tensor(wl.gamma).to(device)
+    return d
+
+
+def call(mf, wl, d, outs, stream=None):
+    mf.moe_finalize(d["x"], d["idx"], d["w"], wl.wkind, d["shared"],
+                    routed_scale=wl.routed_scale, residual=d.get("residual"),
+                    gamma=d.get("gamma"), eps=wl.eps, out=outs.get("out"),
+                    residual_out=outs.get("residual_out"), norm_out=outs.get("norm_out"),
+                    write_out="out" in outs, stream=stream)
+
+
+def time_headline(mf, wl, d, outs, steps, warmup, ws, device):
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        call(mf, wl, d, outs)
+    torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(ws)
+    torch.cuda.synchronize(device)
+    for a, b in ev:
+        a.record(stream)
+        call(mf, wl, d, outs)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(ws)
+    per = [a.elapsed_time(b) for a, b in ev]
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    return total_ms, per
+
+
+def decode_latency(mf, name, device, reps):
+    """µs per call on inputs rotated through copies whose total exceeds L2."""
+    wl = W.make(name)
+    d = device_inputs(wl, device)
+    touched = workload_bytes(wl, True)
+    R = max(2, int(np.ceil(2 * L2_BYTES / touched)))
+    R = min(R, 2048)
+    # R copies of every per-call operand at distinct addresses
+    xs = d["x"].unsqueeze(0).expand(R, *d["x"].shape).contiguous()
+    shs = d["shared"].unsqueeze(0).expand(R, *d["shared"].shape).contiguous()
+    outs = torch.empty((R, wl.T, wl.H), dtype=torch.bfloat16, device=device)
+    sets = [({"x": xs[r], "idx": d["idx"], "w": d["w"], "shared": shs[r]}, {"out": outs[r]})
+            for r in range(R)]
+
+    def one_pass():
+        for dd, oo in sets:
+            call(mf, wl, dd, oo)
+
+    one_pass()
+    torch.cuda.synchronize(device)
+    # eager, back to back
+    n_pass = max(1, reps // R)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n_pass):
+        one_pass()
+    b.record()
+    torch.cuda.synchronize(device)
+    eager_us = a.elapsed_time(b) * 1e3 / (n_pass * R)
+    # CUDA graph of one pass over all copies, replayed
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            one_pass()
+    torch.cuda.current_stream(device).wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize(device)
+    samples = []
+    for _ in range(5):
+        a.record()
+        for _ in range(n_pass):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize(device)
+        samples.append(a.elapsed_time(b) * 1e3 / (n_pass * R))
+    graph_us = statistics.median(samples)
+    plan = mf.plan(wl.T, wl.K, wl.H, False, True,
+                   torch.cuda.get_device_properties(device).multi_processor_count)
+    del xs, shs, outs, g
+    return {"T": wl.T, "K": wl.K, "H": wl.H, "routing": wl.wkind,
+            "us_per_call_graph": round(graph_us, 3), "us_per_call_eager": round(eager_us, 3),
+            "GBps_graph": round(touched / (graph_us * 1e-6) / 1e9, 1),
+            "copies": R, "calls": n_pass * R, "plan": plan}
+
+
+def e2e(mf, wl, host, device, steps):
+    """GB/s with host inputs: per step, H2D of every input, the call, D2H of
+    the results, all inside the timed region."""
+    d = device_inputs(wl, device)
+    outs = {"residual_out": torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device),
+            "norm_out": torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device)}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def step():
+        for k, t in host.items():
+            d[k].copy_(t, non_blocking=True)
+        call(mf, wl, d, outs)
+        for k, t in outs.items():
+            host_out[k].copy_(t, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------- CPU baseline
+
+
+def oracle_gbps(wl, tokens, repeat_until_s=0.0):
+    """fp64 oracle over the given token rows; returns (GB/s, seconds, passes)."""
+    import oracle   # test infrastructure: timed here, never used by the GPU path
+    orc = oracle.default()
+    sub = dict(idx=wl.idx[tokens], weights=np.ascontiguousarray(wl.weights[tokens]),
+               shared=wl.shared[tokens],
+               residual=None if wl.residual is None else wl.residual[tokens])
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        orc.moe_finalize(wl.permuted_out, sub["idx"], sub["weights"], wl.wkind,
+                         wl.routed_scale, sub["shared"], sub["residual"], wl.gamma, wl.eps,
+                         want_out=False)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= repeat_until_s or passes >= 3:
+            break
+    nbytes = algorithmic_bytes(len(tokens), wl.K, wl.H, 4, wl.with_norm, False)
+    return nbytes * passes / el / 1e9, el / passes, passes
+
+
+# ------------------------------------------------------------------- main
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    wl = W.make(WORKLOAD)
+    # per step a token sample sized so that all steps take about a minute
+    per_token_s = 4e-4
+    n_tok = int(np.clip(60.0 / max(1, args.steps + args.warmup) / per_token_s, 8, wl.T))
+    starts = [(i * n_tok) % (wl.T - n_tok + 1) for i in range(args.steps + args.warmup)]
+    times = []
+    for i, s0 in enumerate(starts):
+        toks = np.arange(s0, s0 + n_tok)
+        _, sec, _ = oracle_gbps(wl, toks)
+        if i >= args.warmup:
+            times.append(sec)
+    nbytes = algorithmic_bytes(n_tok, wl.K, wl.H, 4, True, False)
+    ms = 1e3 * sum(times) / len(times)
+    value = nbytes / (ms * 1e-3) / 1e9
+    sample = f"{n_tok} consecutive tokens of {WORKLOAD} per step, full rows"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": wl.T, "K": wl.K, "H": wl.H, "E": wl.E,
+                       "P": wl.P, "tokens_per_step": n_tok},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, ws, rank, local):
+    from moe_deferred_finalize_gb300 import build
+    build.build_library()          # no-op when already built; there is no fallback
+    import moe_deferred_finalize_gb300 as mf
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wl = W.make(WORKLOAD, alloc=pinned_alloc)
+    d = device_inputs(wl, device)
+    outs = {"residual_out": torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device),
+            "norm_out": torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device)}
+    nbytes = workload_bytes(wl, write_out=False)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    plan = mf.plan(wl.T, wl.K, wl.H, True, True, sms)
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    if rank == 0:
+        sampler.start()
+    total_ms, per = time_headline(mf, wl, d, outs, args.steps, args.warmup, ws, device)
+    clocks = sampler.stop() if rank == 0 else None
+
+    ms_step = max_over_ranks(total_ms / args.steps, ws)
+    kernel_ms = statistics.mean(per)
+    value = sum_over_ranks(nbytes, ws) / (ms_step * 1e-3) / 1e9
+
+    peak, peak_src = measured_peaks()
+    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+    traffic = recorded_traffic()
+
+    host = {"x": host_tensor(wl.permuted_out), "idx": host_tensor(wl.idx),
+            "w": host_tensor(np.ascontiguousarray(wl.weights)), "shared": host_tensor(wl.shared),
+            "residual": host_tensor(wl.residual), "gamma": host_tensor(wl.gamma)}
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_ms, h2d, d2h = e2e(mf, wl, host, device, e2e_steps)
+    e2e_ms = max_over_ranks(e2e_ms, ws)
+    e2e_value = sum_over_ranks(nbytes, ws) / (e2e_ms * 1e-3) / 1e9
+
+    del d, outs
+    torch.cuda.empty_cache()
+    decode = {}
+    if not args.skip_decode:
+        decode = {"T1": decode_latency(mf, "decode_bs1_packed", device, 4000),
+                  "T256": decode_latency(mf, "decode_bs256", device, 2000)}
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        gbps, sec, passes = oracle_gbps(wl, np.arange(wl.T), repeat_until_s=10.0)
+        cpu = {"value": round(gbps, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"all {wl.T} tokens of {WORKLOAD}, {passes} pass(es), "
+                         f"{sec:.2f} s per pass, single-threaded fp64"}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": wl.T, "K": wl.K, "H": wl.H, "E": wl.E,
+                   "P": wl.P, "routing": "fp32 normalised sigmoid", "routed_scale": 2.5,
+                   "rmsnorm": True, "emits": ["residual_out", "norm_out"], "io": "bf16",
+                   "bytes_per_step": nbytes, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (%.2f GB read per step)" % (
+                       (nbytes - 2 * wl.T * wl.H * 2) / 1e9),
+                   "plan": plan},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": peak_src, "kernel_ms": round(kernel_ms, 5)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": round(e2e_ms, 3)},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "decode": decode,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-decode", action="store_true", help="omit the decode latency lines")
+    ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU oracle baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            return run_reference(args, ws, rank)
+        return run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,214 @@
+/*
+ * moe_finalize.h -- C ABI of the deferred MoE finalize library
+ * (libmoe_finalize.so), hand-written CUDA for sm_103a.
+ *
+ * The operation.  A mixture-of-experts layer whose expert kernel skips its
+ * own top-k combine leaves behind unweighted expert outputs, one row per
+ * (token, slot), grouped by expert and padded per expert ("Support deferred
+ * MoE finalize for MXFP4 and FP8 block-scale", Motivation; "[Kimi K2.5] Fuse
+ * deferred MoE finalize into next-layer AR + residual + RMSNorm", Numerics &
+ * speed: the padded permuted gemm2_out that the index map gathers from).
+ * The finalize then does, per token t and hidden column h, in one pass:
+ *
+ *   m[t,h]            = sum_k (w[t,k] * routed_scale) * permuted_out[idx[t,k], h]
+ *                       + shared_out[t,h]
+ *   out[t,h]          = bf16(m)
+ *   with a residual:
+ *   s[t,h]            = m + residual[t,h]
+ *   residual_out[t,h] = bf16(s)
+ *   norm_out[t,h]     = bf16(r * inv * gamma[h]),  r = residual_out[t,h],
+ *                       inv = 1 / sqrt(mean_h(r^2) + eps)
+ *
+ * Sources: the weighted combine merged with the shared-expert add
+ * ("Support deferred MoE finalize ...", Motivation); the routed scaling
+ * factor multiplied into the weight held in a register, 1.0 for callers
+ * without one (same page, Modifications item 2); residual add + RMSNorm
+ * with residual_out kept, and the [token, top_k] shape of the index map and
+ * weights ("[Kimi K2.5] Fuse deferred MoE finalize ...", Summary and Key
+ * modifications); fp32 or bf16 routing weights and the packed
+ * (expert_id << 16) | bf16(weight) words ("[Deepseek V4] Keep fp32 routing
+ * weights in the mxfp4 trtllm MoE", description).
+ *
+ * Arithmetic: all sums in fp32 registers, one round-to-nearest-even to bf16
+ * per output.  The norm is computed from the bf16-rounded residual_out, so a
+ * consumer holding only residual_out can reproduce norm_out.
+ *
+ * Conventions for every entry point:
+ *   - all array pointers are DEVICE pointers unless stated otherwise;
+ *     bf16 arrays are raw IEEE bfloat16 bit patterns (uint16_t storage);
+ *   - all arrays are dense, row-major, with no padding between rows;
+ *   - the caller owns every buffer; the library allocates no memory, never
+ *     synchronises the device or the stream, and keeps no per-call state;
+ *     work is enqueued on `stream` and the call returns at once;
+ *   - argument errors are detected on the host before anything is enqueued
+ *     and returned as a status; nothing is launched then;
+ *   - kernels never trap: an index outside [0, P) is a contract violation
+ *     (undefined results), detectable beforehand with
+ *     moe_finalize_check_indices;
+ *   - MOEF_ERR_CUDA means the CUDA runtime refused a launch or a query.
+ */
+#ifndef MOE_FINALIZE_H_
+#define MOE_FINALIZE_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Encoding of the routing-weight operand [T, K].  Exactly one encoding is
+ * accepted per call; it is never inferred from the bytes (reading fp32
+ * weights as bf16 is the failure reported in "[Deepseek V4] Keep fp32
+ * routing weights in the mxfp4 trtllm MoE", revert note). */
+typedef enum {
+    MOEF_W_FP32 = 0,        /* float32 weights                                  */
+    MOEF_W_BF16 = 1,        /* bfloat16 bit patterns, widened exactly to fp32    */
+    MOEF_W_PACKED_TOPK = 2  /* int32 (expert_id << 16) | bf16(weight); the       */
+                            /* weight is the low half, the expert id is unused   */
+} moef_weight_kind;
+
+typedef enum {
+    MOEF_OK = 0,
+    MOEF_ERR_NULL = 1,   /* a required pointer is NULL                          */
+    MOEF_ERR_SHAPE = 2,  /* a size is out of range                              */
+    MOEF_ERR_ALIGN = 3,  /* a pointer is not aligned to its element size        */
+    MOEF_ERR_ARG = 4,    /* an enum, a scalar or an optional-argument pairing   */
+    MOEF_ERR_CUDA = 5,   /* the CUDA runtime returned an error                  */
+    MOEF_ERR_INDEX = 6   /* reserved for index errors reported by callers       */
+} moef_status;
+
+/* Largest top_k accepted. */
+#define MOEF_MAX_K 32
+
+/*
+ * moe_finalize -- the deferred finalize (see the file comment).
+ *
+ *   permuted_out  bf16 [P, H]  unweighted expert rows, padded per expert;
+ *                              padding rows are never read
+ *   P             rows of permuted_out (>= 1); used for argument checks and
+ *                              by moe_finalize_check_indices
+ *   idx_map       int32 [T, K] row of permuted_out for slot (t, k)
+ *                              (expanded_idx_to_permuted_idx); every entry
+ *                              must lie in [0, P)
+ *   weights       [T, K]       routing weights, encoding given by wkind
+ *   routed_scale  multiplies every routing weight (1.0 when unused)
+ *   shared_out    bf16 [T, H]  shared-expert output, required
+ *   residual      bf16 [T, H]  optional; residual and gamma go together
+ *   gamma         bf16 [H]     RMSNorm weight, optional
+ *   eps           RMSNorm epsilon (>= 0); ignored without a residual
+ *   out           bf16 [T, H]  finalized MoE output; may be NULL only when a
+ *                              residual is given (then only residual_out and
+ *                              norm_out are written)
+ *   residual_out  bf16 [T, H]  required iff residual is given
+ *   norm_out      bf16 [T, H]  required iff residual is given
+ *   T             tokens (>= 0; T = 0 returns MOEF_OK and enqueues nothing)
+ *   K             top_k, 1 <= K <= MOEF_MAX_K
+ *   H             hidden size (>= 1)
+ *   stream        CUDA stream to enqueue on (0 = legacy default stream)
+ *
+ * In place: out may equal shared_out and residual_out may equal residual
+ * (each element is read before it is written, by the same thread).  No
+ * other overlap between outputs and inputs is allowed.
+ *
+ * Alignment: bf16 pointers must be 2-byte aligned, idx_map and fp32/packed
+ * weights 4-byte aligned (else MOEF_ERR_ALIGN).  The 16-byte vector path
+ * is used when H % 8 == 0 and every bf16 pointer is 16-byte aligned; any
+ * other case takes a scalar path with the same results.
+ *
+ * The call allocates nothing and does not synchronise, so it may be
+ * captured in a CUDA graph ("[Kimi K2.5] Fuse deferred MoE finalize ...",
+ * Key modifications: workspace sized before capture, never grown inside
+ * captured graphs).  Its first call on a device with a given RMSNorm split
+ * wider than 8 CTAs sets a kernel attribute; make that first call before
+ * any capture.
+ */
+moef_status moe_finalize(const void *permuted_out, int64_t P,
+                         const int32_t *idx_map,
+                         const void *weights, moef_weight_kind wkind,
+                         float routed_scale,
+                         const void *shared_out,
+                         const void *residual, const void *gamma, float eps,
+                         void *out, void *residual_out, void *norm_out,
+                         int T, int K, int H, cudaStream_t stream);
+
+/*
+ * Launch plan of moe_finalize: how a call is split over CTAs.  Each token
+ * row is cut into `splits` slices of `slice` vectors of `vec` bf16 values;
+ * one CTA of `threads` threads finalizes one slice, each thread handling up
+ * to `vpt` vectors.  With a residual and splits > 1 the CTAs of one token
+ * form a thread-block cluster of size `splits` and combine their partial
+ * sums of squares through distributed shared memory.
+ */
+typedef struct {
+    int vec;        /* bf16 values per vector: 8 (16-byte path) or 1 (scalar)  */
+    int splits;     /* CTAs per token                                         */
+    int slice;      /* vectors per CTA (the last CTA of a token may have fewer) */
+    int threads;    /* threads per CTA                                        */
+    int vpt;        /* vectors per thread per pass (1, 2, 4 or 8)              */
+    int cluster;    /* cluster size along x (1 = no cluster)                   */
+    int64_t grid;   /* CTAs launched = T * splits                              */
+} moef_plan;
+
+/*
+ * moe_finalize_plan -- the plan moe_finalize uses (pure host computation,
+ * no CUDA call).  with_norm: a residual is given; vec_ok: the 16-byte path
+ * applies (H % 8 == 0 and 16-byte aligned pointers); num_sms: multiprocessor
+ * count of the device.  splits_hint / threads_hint: 0 for the automatic
+ * choice, else the requested value (validated).  Returns MOEF_ERR_SHAPE if
+ * the sizes cannot be served (e.g. an RMSNorm row too long for one cluster),
+ * MOEF_ERR_ARG for a bad hint.
+ */
+moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok,
+                              int num_sms, int splits_hint, int threads_hint,
+                              moef_plan *plan);
+
+/*
+ * moe_finalize_ex -- moe_finalize with launch hints (0 = automatic), for
+ * callers that pin a launch shape (e.g. one captured graph for several
+ * batch sizes) and for tuning.  Same arguments and rules otherwise.
+ */
+moef_status moe_finalize_ex(const void *permuted_out, int64_t P,
+                            const int32_t *idx_map,
+                            const void *weights, moef_weight_kind wkind,
+                            float routed_scale,
+                            const void *shared_out,
+                            const void *residual, const void *gamma, float eps,
+                            void *out, void *residual_out, void *norm_out,
+                            int T, int K, int H,
+                            int splits_hint, int threads_hint,
+                            cudaStream_t stream);
+
+/*
+ * unpack_topk_ids -- split n packed routing words (expert_id << 16) |
+ * bf16(weight) ("[Deepseek V4] Keep fp32 routing weights in the mxfp4
+ * trtllm MoE", description) into expert ids (the high 16 bits as an
+ * unsigned field, 0..65535) and fp32 weights (the low 16 bits widened
+ * exactly).  Bit-exact.  packed: int32 [n]; expert_ids: int32 [n] or NULL;
+ * weights_f32: float [n] or NULL (at least one non-NULL).  n = 0 returns
+ * MOEF_OK and enqueues nothing.  The three arrays must not overlap.
+ */
+moef_status unpack_topk_ids(const int32_t *packed, int64_t n,
+                            int32_t *expert_ids, float *weights_f32,
+                            cudaStream_t stream);
+
+/*
+ * moe_finalize_check_indices -- count the entries of idx_map [T, K] that
+ * lie outside [0, P) (the out-of-bounds class named in "[Kimi K2.5] Fuse
+ * deferred MoE finalize ...", Key modifications: a flat index map read
+ * with the wrong top_k).  d_bad_count: one caller-owned device int32; it is
+ * zeroed on `stream` and then receives the count.  Enqueued work only: read
+ * the count after synchronising the stream.
+ */
+moef_status moe_finalize_check_indices(const int32_t *idx_map, int T, int K,
+                                       int64_t P, int32_t *d_bad_count,
+                                       cudaStream_t stream);
+
+/* Static English text for a status value (never NULL). */
+const char *moef_status_string(moef_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FINALIZE_H_ */

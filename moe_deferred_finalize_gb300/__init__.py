@@ -1,0 +1,14 @@
+"""GB300-native deferred MoE finalize.
+
+The finalize gathers each token's top-k unweighted expert rows from the
+padded, permuted expert output, weights them (fp32, bf16 or packed routing
+weights times a routed scale), adds the shared-expert output and optionally
+the residual followed by RMSNorm, in one CUDA kernel for sm_103a.  The
+kernels and their C ABI live in ``libmoe_finalize.so``
+(``include/moe_finalize.h``); this package is its thin Python binding.
+"""
+from ._abi import (WKIND, MoefError, check_indices, lib, moe_finalize, plan,  # noqa: F401
+                   unpack_topk_ids)
+
+__all__ = ["moe_finalize", "unpack_topk_ids", "check_indices", "plan", "lib", "MoefError",
+           "WKIND"]

@@ -1,0 +1,216 @@
+"""ctypes binding of libmoe_finalize.so (declared in include/moe_finalize.h).
+
+Argument marshalling only: shape/dtype checks, output allocation through
+torch, the current CUDA stream, and status -> exception.  Every step of the
+finalize runs in the library's CUDA kernels; there is no other code path,
+and calls fail loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_finalize.so")
+
+WKIND = {"fp32": 0, "bf16": 1, "packed": 2}
+_WDTYPE = {"fp32": (torch.float32,), "bf16": (torch.bfloat16, torch.int16),
+           "packed": (torch.int32,)}
+
+STATUS = {0: "MOEF_OK", 1: "MOEF_ERR_NULL", 2: "MOEF_ERR_SHAPE", 3: "MOEF_ERR_ALIGN",
+          4: "MOEF_ERR_ARG", 5: "MOEF_ERR_CUDA", 6: "MOEF_ERR_INDEX"}
+
+
+class MoefError(RuntimeError):
+    """A non-OK status from the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        text = _lib().moef_status_string(status).decode()
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({text})")
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("vec", ctypes.c_int), ("splits", ctypes.c_int), ("slice", ctypes.c_int),
+                ("threads", ctypes.c_int), ("vpt", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("grid", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "libmoe_finalize.so is not built (there is no fallback path); build it with "
+                "`python -m moe_deferred_finalize_gb300.build` or __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        common = [vp, i64, vp, vp, i32, f32, vp, vp, vp, f32, vp, vp, vp, i32, i32, i32]
+        lib.moe_finalize.argtypes = common + [vp]
+        lib.moe_finalize.restype = i32
+        lib.moe_finalize_ex.argtypes = common + [i32, i32, vp]
+        lib.moe_finalize_ex.restype = i32
+        lib.moe_finalize_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
+                                          ctypes.POINTER(Plan)]
+        lib.moe_finalize_plan.restype = i32
+        lib.unpack_topk_ids.argtypes = [vp, i64, vp, vp, vp]
+        lib.unpack_topk_ids.restype = i32
+        lib.moe_finalize_check_indices.argtypes = [vp, i32, i32, i64, vp, vp]
+        lib.moe_finalize_check_indices.restype = i32
+        lib.moef_status_string.argtypes = [i32]
+        lib.moef_status_string.restype = ctypes.c_char_p
+        _LIB = lib
+    return _LIB
+
+
+def lib():
+    """The loaded ctypes library (raw C ABI)."""
+    return _lib()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(t, name, dtypes, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_BF16 = (torch.bfloat16,)
+
+
+def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: torch.Tensor,
+                 wkind: str, shared_out: torch.Tensor, *, routed_scale: float = 1.0,
+                 residual: Optional[torch.Tensor] = None, gamma: Optional[torch.Tensor] = None,
+                 eps: float = 1e-6, out: Optional[torch.Tensor] = None,
+                 residual_out: Optional[torch.Tensor] = None,
+                 norm_out: Optional[torch.Tensor] = None, write_out: bool = True,
+                 splits: int = 0, threads: int = 0, stream=None) -> dict:
+    """Deferred MoE finalize on the GPU (see include/moe_finalize.h).
+
+    permuted_out bf16 [P, H]; idx_map int32 [T, K]; weights [T, K] encoded
+    as ``wkind`` ("fp32": float32, "bf16": bfloat16, "packed": int32 words
+    (expert_id << 16) | bf16(weight)); shared_out bf16 [T, H]; optional
+    residual bf16 [T, H] with gamma bf16 [H].  Outputs are allocated when not
+    given; with a residual, ``write_out=False`` skips ``out``.  Returns a dict
+    with "out" and, with a residual, "residual_out" and "norm_out".
+    Enqueued on the current stream (or ``stream``); nothing is synchronised.
+    """
+    if wkind not in WKIND:
+        raise ValueError(f"wkind must be one of {sorted(WKIND)}")
+    device = permuted_out.device
+    if device.type != "cuda":
+        raise ValueError("permuted_out must be a CUDA tensor")
+    if permuted_out.dim() != 2 or idx_map.dim() != 2:
+        raise ValueError("permuted_out is [P, H] and idx_map is [T, K]")
+    P, H = permuted_out.shape
+    T, K = idx_map.shape
+    _check(permuted_out, "permuted_out", _BF16, (P, H), device)
+    _check(idx_map, "idx_map", (torch.int32,), (T, K), device)
+    _check(weights, "weights", _WDTYPE[wkind], (T, K), device)
+    _check(shared_out, "shared_out", _BF16, (T, H), device)
+    norm = residual is not None
+    if norm != (gamma is not None):
+        raise ValueError("residual and gamma go together")
+    if norm:
+        _check(residual, "residual", _BF16, (T, H), device)
+        _check(gamma, "gamma", _BF16, (H,), device)
+        if residual_out is None:
+            residual_out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        if norm_out is None:
+            norm_out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        _check(residual_out, "residual_out", _BF16, (T, H), device)
+        _check(norm_out, "norm_out", _BF16, (T, H), device)
+    elif residual_out is not None or norm_out is not None:
+        raise ValueError("residual_out / norm_out need a residual")
+    if not norm or write_out:
+        if out is None:
+            out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        _check(out, "out", _BF16, (T, H), device)
+    else:
+        out = None
+
+    st = _lib().moe_finalize_ex(
+        _ptr(permuted_out), P, _ptr(idx_map), _ptr(weights), WKIND[wkind],
+        float(routed_scale), _ptr(shared_out), _ptr(residual), _ptr(gamma), float(eps),
+        _ptr(out), _ptr(residual_out), _ptr(norm_out), T, K, H, int(splits), int(threads),
+        _stream(stream, device))
+    if st != 0:
+        raise MoefError(st, "moe_finalize")
+    res = {"out": out}
+    if norm:
+        res["residual_out"] = residual_out
+        res["norm_out"] = norm_out
+    return res
+
+
+def plan(T: int, K: int, H: int, with_norm: bool, vec_ok: bool = True, num_sms: int = 152,
+         splits: int = 0, threads: int = 0) -> dict:
+    """The launch plan moe_finalize uses for these sizes (host computation only)."""
+    p = Plan()
+    st = _lib().moe_finalize_plan(T, K, H, int(with_norm), int(vec_ok), num_sms, splits,
+                                  threads, ctypes.byref(p))
+    if st != 0:
+        raise MoefError(st, "moe_finalize_plan")
+    return p.as_dict()
+
+
+def unpack_topk_ids(packed: torch.Tensor, expert_ids: Optional[torch.Tensor] = None,
+                    weights: Optional[torch.Tensor] = None, stream=None):
+    """Packed int32 words -> (expert ids int32, weights float32), same shape."""
+    if packed.device.type != "cuda" or packed.dtype != torch.int32 or not packed.is_contiguous():
+        raise ValueError("packed must be a contiguous int32 CUDA tensor")
+    device = packed.device
+    if expert_ids is None:
+        expert_ids = torch.empty_like(packed)
+    if weights is None:
+        weights = torch.empty(packed.shape, dtype=torch.float32, device=device)
+    _check(expert_ids, "expert_ids", (torch.int32,), packed.shape, device)
+    _check(weights, "weights", (torch.float32,), packed.shape, device)
+    st = _lib().unpack_topk_ids(_ptr(packed), packed.numel(), _ptr(expert_ids), _ptr(weights),
+                                _stream(stream, device))
+    if st != 0:
+        raise MoefError(st, "unpack_topk_ids")
+    return expert_ids, weights
+
+
+def check_indices(idx_map: torch.Tensor, P: int, counter: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """Enqueue a count of idx_map entries outside [0, P); returns the device
+    int32 [1] counter (read it after the stream has run)."""
+    if idx_map.dim() != 2 or idx_map.dtype != torch.int32 or not idx_map.is_contiguous():
+        raise ValueError("idx_map must be a contiguous int32 [T, K] tensor")
+    device = idx_map.device
+    if counter is None:
+        counter = torch.empty(1, dtype=torch.int32, device=device)
+    T, K = idx_map.shape
+    st = _lib().moe_finalize_check_indices(_ptr(idx_map), T, K, int(P), _ptr(counter),
+                                           _stream(stream, device))
+    if st != 0:
+        raise MoefError(st, "moe_finalize_check_indices")
+    return counter

@@ -1,0 +1,233 @@
+// C ABI of libmoe_finalize.so: argument checks, launch planning and the
+// entry points declared in moe_finalize.h.  Host code only; every step of
+// the computation runs in the kernels of finalize.cu and routing.cu.
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.cuh"
+
+namespace {
+
+constexpr int kMaxThreads = 256;   // matches the kernels' launch bounds
+constexpr int kMaxVpt = 8;
+constexpr int kMaxCluster = 16;    // non-portable cluster size limit
+constexpr int kMaxDevices = 64;
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+// Smallest supported vectors-per-thread count >= need (1, 2, 4 or 8), or
+// need itself when it is larger than 8.
+int vpt_bucket(int need) {
+    if (need <= 1) return 1;
+    if (need <= 2) return 2;
+    if (need <= 4) return 4;
+    if (need <= 8) return 8;
+    return need;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Multiprocessor count of the current device, cached per device.
+cudaError_t current_sms(int *sms) {
+    static int cache[kMaxDevices];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) {
+        *sms = cache[dev];
+        return cudaSuccess;
+    }
+    int n = 0;
+    err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev] = n;
+    *sms = n;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moef_status_string(moef_status s) {
+    switch (s) {
+        case MOEF_OK: return "ok";
+        case MOEF_ERR_NULL: return "a required pointer is NULL";
+        case MOEF_ERR_SHAPE: return "a size is out of range";
+        case MOEF_ERR_ALIGN: return "a pointer is not aligned to its element size";
+        case MOEF_ERR_ARG: return "invalid argument (enum, scalar or optional-argument pairing)";
+        case MOEF_ERR_CUDA: return "the CUDA runtime returned an error";
+        case MOEF_ERR_INDEX: return "an index lies outside [0, P)";
+    }
+    return "unknown status";
+}
+
+// Plan choice.  Two regimes:
+//  * latency: while one 16-byte vector per thread fits in about two waves of
+//    fully occupied SMs, every thread takes one vector (vpt = 1) and a row
+//    is cut into 128-vector slices, one CTA each.  This puts every gathered
+//    load of the call in flight at once, which is what decode batch sizes
+//    need (the time is a few memory latencies, not bytes).
+//  * bandwidth: otherwise one CTA of 128 (or 256) threads owns a whole row,
+//    each thread several vectors, and the grid has one CTA per token.
+// With RMSNorm a row must fit one pass of one CTA (at most 256 x 8
+// vectors), or one cluster of at most 16 CTAs.
+moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, int num_sms,
+                              int splits_hint, int threads_hint, moef_plan *plan) {
+    if (!plan) return MOEF_ERR_NULL;
+    if (T < 0 || K < 1 || K > MOEF_MAX_K || H < 1) return MOEF_ERR_SHAPE;
+    if (num_sms < 1 || splits_hint < 0 || threads_hint < 0) return MOEF_ERR_ARG;
+    if (threads_hint && (threads_hint > kMaxThreads || threads_hint % 32)) return MOEF_ERR_ARG;
+
+    const int vec = (vec_ok && H % 8 == 0) ? 8 : 1;
+    const int nvec = H / vec;
+
+    int splits;
+    if (splits_hint) {
+        splits = splits_hint < nvec ? splits_hint : nvec;
+    } else {
+        const int64_t one_per_thread = static_cast<int64_t>(T) * nvec;
+        const int64_t two_waves = static_cast<int64_t>(num_sms) * 2048 * 2;
+        splits = (one_per_thread <= two_waves) ? ceil_div(nvec, 128) : 1;
+        if (!threads_hint && splits == 1 && with_norm && nvec > kMaxThreads * kMaxVpt)
+            splits = ceil_div(nvec, kMaxThreads * kMaxVpt);
+        if (with_norm && splits > kMaxCluster) splits = kMaxCluster;
+    }
+    if (with_norm && splits > kMaxCluster) return MOEF_ERR_ARG;
+
+    const int slice = ceil_div(nvec, splits);
+    splits = ceil_div(nvec, slice);   // no empty CTAs
+
+    int threads;
+    if (threads_hint) {
+        threads = threads_hint;
+    } else {
+        const int cap = splits > 1 ? kMaxThreads : 128;
+        threads = round_up(slice < cap ? slice : cap, 32);
+        if (ceil_div(slice, threads) > kMaxVpt) threads = kMaxThreads;
+    }
+    int vpt = vpt_bucket(ceil_div(slice, threads));
+    if (vpt > kMaxVpt) {
+        if (with_norm) return MOEF_ERR_SHAPE;
+        vpt = kMaxVpt;     // several passes over the slice
+    }
+
+    const int64_t grid = static_cast<int64_t>(T) * splits;
+    if (grid > 0x7FFFFFFFLL) return MOEF_ERR_SHAPE;
+
+    plan->vec = vec;
+    plan->splits = splits;
+    plan->slice = slice;
+    plan->threads = threads;
+    plan->vpt = vpt;
+    plan->cluster = (with_norm && splits > 1) ? splits : 1;
+    plan->grid = grid;
+    return MOEF_OK;
+}
+
+moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *idx_map,
+                            const void *weights, moef_weight_kind wkind, float routed_scale,
+                            const void *shared_out, const void *residual, const void *gamma,
+                            float eps, void *out, void *residual_out, void *norm_out,
+                            int T, int K, int H, int splits_hint, int threads_hint,
+                            cudaStream_t stream) {
+    if (T < 0 || K < 1 || K > MOEF_MAX_K || H < 1) return MOEF_ERR_SHAPE;
+    if (wkind != MOEF_W_FP32 && wkind != MOEF_W_BF16 && wkind != MOEF_W_PACKED_TOPK)
+        return MOEF_ERR_ARG;
+    if (splits_hint < 0 || threads_hint < 0) return MOEF_ERR_ARG;
+    if (T == 0) return MOEF_OK;
+    if (P < 1) return MOEF_ERR_SHAPE;
+    if (!permuted_out || !idx_map || !weights || !shared_out) return MOEF_ERR_NULL;
+
+    const bool norm = residual != nullptr;
+    if ((residual == nullptr) != (gamma == nullptr)) return MOEF_ERR_ARG;
+    if (norm) {
+        if (!residual_out || !norm_out) return MOEF_ERR_NULL;
+        if (!(eps >= 0.f) || isinf(eps)) return MOEF_ERR_ARG;
+    } else {
+        if (residual_out || norm_out) return MOEF_ERR_ARG;
+        if (!out) return MOEF_ERR_NULL;
+    }
+
+    const void *bf16_ptrs[] = {permuted_out, shared_out, residual, gamma, out, residual_out,
+                               norm_out};
+    for (const void *q : bf16_ptrs)
+        if (q && !aligned(q, 2)) return MOEF_ERR_ALIGN;
+    if (!aligned(idx_map, 4)) return MOEF_ERR_ALIGN;
+    if (!aligned(weights, wkind == MOEF_W_BF16 ? 2 : 4)) return MOEF_ERR_ALIGN;
+
+    bool vec_ok = (H % 8) == 0;
+    for (const void *q : bf16_ptrs)
+        if (q && !aligned(q, 16)) vec_ok = false;
+
+    int sms = 0;
+    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
+    moef_plan plan;
+    const moef_status st = moe_finalize_plan(T, K, H, norm ? 1 : 0, vec_ok ? 1 : 0, sms,
+                                             splits_hint, threads_hint, &plan);
+    if (st != MOEF_OK) return st;
+
+    moef::FinalizeParams p;
+    p.x = static_cast<const uint16_t *>(permuted_out);
+    p.idx = idx_map;
+    p.weights = weights;
+    p.shared = static_cast<const uint16_t *>(shared_out);
+    p.residual = static_cast<const uint16_t *>(residual);
+    p.gamma = static_cast<const uint16_t *>(gamma);
+    p.out = static_cast<uint16_t *>(out);
+    p.residual_out = static_cast<uint16_t *>(residual_out);
+    p.norm_out = static_cast<uint16_t *>(norm_out);
+    p.routed_scale = routed_scale;
+    p.eps = eps;
+    p.wkind = static_cast<int>(wkind);
+    p.T = T;
+    p.K = K;
+    p.H = H;
+    p.nvec = H / plan.vec;
+    p.splits = plan.splits;
+    p.slice = plan.slice;
+    return moef::launch_finalize(p, plan, stream) == cudaSuccess ? MOEF_OK : MOEF_ERR_CUDA;
+}
+
+moef_status moe_finalize(const void *permuted_out, int64_t P, const int32_t *idx_map,
+                         const void *weights, moef_weight_kind wkind, float routed_scale,
+                         const void *shared_out, const void *residual, const void *gamma,
+                         float eps, void *out, void *residual_out, void *norm_out,
+                         int T, int K, int H, cudaStream_t stream) {
+    return moe_finalize_ex(permuted_out, P, idx_map, weights, wkind, routed_scale, shared_out,
+                           residual, gamma, eps, out, residual_out, norm_out, T, K, H, 0, 0,
+                           stream);
+}
+
+moef_status unpack_topk_ids(const int32_t *packed, int64_t n, int32_t *expert_ids,
+                            float *weights_f32, cudaStream_t stream) {
+    if (n < 0) return MOEF_ERR_SHAPE;
+    if (n == 0) return MOEF_OK;
+    if (!packed || (!expert_ids && !weights_f32)) return MOEF_ERR_NULL;
+    if (!aligned(packed, 4) || (expert_ids && !aligned(expert_ids, 4)) ||
+        (weights_f32 && !aligned(weights_f32, 4)))
+        return MOEF_ERR_ALIGN;
+    int sms = 0;
+    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
+    return moef::launch_unpack(packed, n, expert_ids, weights_f32, sms, stream) == cudaSuccess
+               ? MOEF_OK
+               : MOEF_ERR_CUDA;
+}
+
+moef_status moe_finalize_check_indices(const int32_t *idx_map, int T, int K, int64_t P,
+                                       int32_t *d_bad_count, cudaStream_t stream) {
+    if (T < 0 || K < 1 || K > MOEF_MAX_K || P < 0) return MOEF_ERR_SHAPE;
+    if (!d_bad_count) return MOEF_ERR_NULL;
+    const int64_t n = static_cast<int64_t>(T) * K;
+    if (n > 0 && !idx_map) return MOEF_ERR_NULL;
+    if (!aligned(d_bad_count, 4) || (idx_map && !aligned(idx_map, 4))) return MOEF_ERR_ALIGN;
+    int sms = 0;
+    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
+    return moef::launch_check_indices(idx_map, n, P, d_bad_count, sms, stream) == cudaSuccess
+               ? MOEF_OK
+               : MOEF_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,319 @@
+// Deferred MoE finalize kernel for sm_103a.
+//
+// One CTA finalizes one slice of one token row:
+//
+//   m = sum_k (w[t,k] * routed_scale) * permuted_out[idx[t,k], slice]
+//       + shared_out[t, slice]
+//   out = bf16(m);  with a residual: residual_out = bf16(m + residual),
+//   norm_out = bf16(residual_out * rsqrt(mean(residual_out^2) + eps) * gamma)
+//
+// ("Support deferred MoE finalize for MXFP4 and FP8 block-scale",
+// Motivation and Modifications item 2; "[Kimi K2.5] Fuse deferred MoE
+// finalize into next-layer AR + residual + RMSNorm", Summary.)
+//
+// Memory plan: the path is an HBM-bound gather-reduce (about 0.4 flop per
+// byte), so there is no tensor-core work.  Each thread owns whole 16-byte
+// vectors (8 bf16 values) of the row; for every vector it issues the K
+// gathered-row loads back to back (read-only path, no L1 allocation: each
+// gathered byte is read exactly once), plus the shared and residual loads,
+// and accumulates in fp32 registers.  Outputs are written with streaming
+// stores.  The token's row indices and scaled weights are staged once in
+// shared memory.  With RMSNorm the bf16-rounded residual_out vectors stay in
+// registers between the two passes; the sum of squares is reduced with warp
+// shuffles and shared memory, and across the CTAs of a split row through
+// distributed shared memory of a thread-block cluster (every CTA adds the
+// partials in the same order, so all slices use the same inverse RMS).
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+
+#include "internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace moef {
+namespace {
+
+constexpr int kMaxThreads = 256;
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);   // .x -> low half
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+template <int VEC>
+struct VecOps;
+
+// 16-byte vectors of 8 bf16 values.
+template <>
+struct VecOps<8> {
+    using V = uint4;
+    // Gathered expert rows: read-only for the kernel's lifetime and read once.
+    static __device__ __forceinline__ V load_row(const uint16_t *p) {
+        V r;
+        asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+            : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+            : "l"(p));
+        return r;
+    }
+    // Dense per-token operands (may alias an output when run in place).
+    static __device__ __forceinline__ V load(const uint16_t *p) {
+        return __ldcs(reinterpret_cast<const uint4 *>(p));
+    }
+    // Small operands reused by every token (gamma).
+    static __device__ __forceinline__ V load_reused(const uint16_t *p) {
+        return __ldg(reinterpret_cast<const uint4 *>(p));
+    }
+    static __device__ __forceinline__ void store(uint16_t *p, V v) {
+        __stcs(reinterpret_cast<uint4 *>(p), v);
+    }
+    static __device__ __forceinline__ void to_f32(const V &v, float f[8]) {
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+        f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+        f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+    }
+    static __device__ __forceinline__ V from_f32(const float f[8]) {
+        V v;
+        v.x = pack_bf16x2(f[0], f[1]);
+        v.y = pack_bf16x2(f[2], f[3]);
+        v.z = pack_bf16x2(f[4], f[5]);
+        v.w = pack_bf16x2(f[6], f[7]);
+        return v;
+    }
+};
+
+// Single bf16 values: any H, any 2-byte alignment.
+template <>
+struct VecOps<1> {
+    using V = unsigned short;
+    static __device__ __forceinline__ V load_row(const uint16_t *p) {
+        return __ldg(reinterpret_cast<const unsigned short *>(p));
+    }
+    static __device__ __forceinline__ V load(const uint16_t *p) {
+        return __ldcs(reinterpret_cast<const unsigned short *>(p));
+    }
+    static __device__ __forceinline__ V load_reused(const uint16_t *p) {
+        return __ldg(reinterpret_cast<const unsigned short *>(p));
+    }
+    static __device__ __forceinline__ void store(uint16_t *p, V v) {
+        __stcs(reinterpret_cast<unsigned short *>(p), v);
+    }
+    static __device__ __forceinline__ void to_f32(const V &v, float f[1]) {
+        f[0] = __uint_as_float(static_cast<uint32_t>(v) << 16);
+    }
+    static __device__ __forceinline__ V from_f32(const float f[1]) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(f[0]));
+    }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Routing weight of slot i, decoded exactly to fp32.
+__device__ __forceinline__ float decode_weight(const void *weights, int wkind, int64_t i) {
+    if (wkind == MOEF_W_FP32) return __ldg(static_cast<const float *>(weights) + i);
+    if (wkind == MOEF_W_BF16)
+        return __uint_as_float(
+            static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(weights) + i)) << 16);
+    // packed (expert_id << 16) | bf16(weight): the low half, moved up
+    return __uint_as_float(
+        static_cast<uint32_t>(__ldg(static_cast<const int *>(weights) + i)) << 16);
+}
+
+template <int VPT, int VEC, bool NORM, bool CLUSTER>
+__global__ void __launch_bounds__(kMaxThreads)
+finalize_kernel(const __grid_constant__ FinalizeParams p) {
+    using Ops = VecOps<VEC>;
+    using V = typename Ops::V;
+
+    __shared__ const uint16_t *s_row[MOEF_MAX_K];
+    __shared__ float s_w[MOEF_MAX_K];
+    __shared__ float s_warp[kMaxThreads / 32];
+    __shared__ float s_cta;
+
+    const int S = p.splits;
+    const int t = blockIdx.x / S;
+    const int split = blockIdx.x - t * S;
+    const int K = p.K;
+    const int nt = blockDim.x;
+
+    // Stage the token's row pointers and scaled weights (the routed scale
+    // folded into the weight once, "Support deferred MoE finalize ...",
+    // Modifications item 2).
+    if (threadIdx.x < K) {
+        const int64_t i = static_cast<int64_t>(t) * K + threadIdx.x;
+        const int r = __ldg(p.idx + i);
+        s_row[threadIdx.x] = p.x + static_cast<int64_t>(r) * p.H;
+        s_w[threadIdx.x] = decode_weight(p.weights, p.wkind, i) * p.routed_scale;
+    }
+    __syncthreads();
+
+    const int64_t tok = static_cast<int64_t>(t) * p.H;
+    const int v_begin = split * p.slice;
+    const int v_end = min(v_begin + p.slice, p.nvec);
+
+    float ss = 0.f;
+    V keep[NORM ? VPT : 1];
+
+    for (int base = v_begin; base < v_end; base += nt * VPT) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = base + threadIdx.x + j * nt;
+            if (v < v_end) {
+                const int64_t e = static_cast<int64_t>(v) * VEC;
+                const V sh = Ops::load(p.shared + tok + e);
+                V rs;
+                if (NORM) rs = Ops::load(p.residual + tok + e);
+
+                float acc[VEC];
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) acc[q] = 0.f;
+                for (int k0 = 0; k0 < K; k0 += 8) {
+                    V xv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (k0 + u < K) xv[u] = Ops::load_row(s_row[k0 + u] + e);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (k0 + u < K) {
+                            float xf[VEC];
+                            Ops::to_f32(xv[u], xf);
+                            const float w = s_w[k0 + u];
+#pragma unroll
+                            for (int q = 0; q < VEC; ++q) acc[q] = fmaf(w, xf[q], acc[q]);
+                        }
+                    }
+                }
+                float f[VEC];
+                Ops::to_f32(sh, f);
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) acc[q] += f[q];
+                if (p.out) Ops::store(p.out + tok + e, Ops::from_f32(acc));
+                if (NORM) {
+                    Ops::to_f32(rs, f);
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) acc[q] += f[q];
+                    const V sv = Ops::from_f32(acc);
+                    Ops::store(p.residual_out + tok + e, sv);
+                    keep[j] = sv;
+                    Ops::to_f32(sv, f);
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) ss = fmaf(f[q], f[q], ss);
+                }
+            }
+        }
+        if (NORM) break;   // the plan gives a norm row slice one pass
+    }
+
+    if constexpr (NORM) {
+        // gamma loads go out before the reductions so their latency overlaps
+        V g[VPT];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = v_begin + threadIdx.x + j * nt;
+            if (v < v_end) g[j] = Ops::load_reused(p.gamma + static_cast<int64_t>(v) * VEC);
+        }
+
+        ss = warp_sum(ss);
+        if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
+        __syncthreads();
+        float total = 0.f;
+        const int nw = (nt + 31) >> 5;
+        for (int w = 0; w < nw; ++w) total += s_warp[w];
+
+        if constexpr (CLUSTER) {
+            cg::cluster_group cluster = cg::this_cluster();
+            if (threadIdx.x == 0) s_cta = total;
+            cluster.sync();
+            total = 0.f;
+            for (int r = 0; r < S; ++r) total += *cluster.map_shared_rank(&s_cta, r);
+            // No CTA may leave while another still reads its s_cta: arrive
+            // now, wait after the stores below.
+            asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+        }
+
+        const float inv = rsqrtf(total / static_cast<float>(p.H) + p.eps);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = v_begin + threadIdx.x + j * nt;
+            if (v < v_end) {
+                float sf[VEC], gf[VEC];
+                Ops::to_f32(keep[j], sf);
+                Ops::to_f32(g[j], gf);
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) sf[q] = sf[q] * inv * gf[q];
+                Ops::store(p.norm_out + tok + static_cast<int64_t>(v) * VEC, Ops::from_f32(sf));
+            }
+        }
+        if constexpr (CLUSTER) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    }
+}
+
+template <int VPT, int VEC, bool NORM, bool CLUSTER>
+cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, cudaStream_t stream) {
+    auto kern = finalize_kernel<VPT, VEC, NORM, CLUSTER>;
+    cudaLaunchAttribute attr[1];
+    unsigned num_attrs = 0;
+    if (CLUSTER) {
+        if (plan.cluster > 8) {
+            // Clusters of 9..16 CTAs are opt-in per kernel and device.
+            static int enabled[64];
+            int dev = 0;
+            cudaError_t err = cudaGetDevice(&dev);
+            if (err != cudaSuccess) return err;
+            if (dev >= 64) return cudaErrorInvalidDevice;
+            if (!enabled[dev]) {
+                err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (err != cudaSuccess) return err;
+                enabled[dev] = 1;
+            }
+        }
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(plan.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        num_attrs = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(plan.threads));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = num_attrs;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int VPT, int VEC>
+cudaError_t launch_v(const FinalizeParams &p, const moef_plan &plan, cudaStream_t stream) {
+    if (!p.residual) return launch_t<VPT, VEC, false, false>(p, plan, stream);
+    if (plan.cluster > 1) return launch_t<VPT, VEC, true, true>(p, plan, stream);
+    return launch_t<VPT, VEC, true, false>(p, plan, stream);
+}
+
+template <int VEC>
+cudaError_t launch_vec(const FinalizeParams &p, const moef_plan &plan, cudaStream_t stream) {
+    switch (plan.vpt) {
+        case 1: return launch_v<1, VEC>(p, plan, stream);
+        case 2: return launch_v<2, VEC>(p, plan, stream);
+        case 4: return launch_v<4, VEC>(p, plan, stream);
+        case 8: return launch_v<8, VEC>(p, plan, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan, cudaStream_t stream) {
+    if (plan.vec == 8) return launch_vec<8>(p, plan, stream);
+    if (plan.vec == 1) return launch_vec<1>(p, plan, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moef

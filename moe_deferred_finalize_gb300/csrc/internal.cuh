@@ -1,0 +1,43 @@
+// Internal declarations shared by the kernel and host translation units of
+// libmoe_finalize.so.  Not part of the public ABI (that is moe_finalize.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_finalize.h"
+
+namespace moef {
+
+// Everything one finalize launch needs, passed by value as the kernel's
+// single parameter (fits the 4 KB parameter space many times over).
+struct FinalizeParams {
+    const uint16_t *x;          // permuted_out, bf16 [P, H]
+    const int32_t *idx;         // [T, K]
+    const void *weights;        // [T, K], encoding in wkind
+    const uint16_t *shared;     // bf16 [T, H]
+    const uint16_t *residual;   // bf16 [T, H] or null
+    const uint16_t *gamma;      // bf16 [H] or null
+    uint16_t *out;              // bf16 [T, H] or null
+    uint16_t *residual_out;     // bf16 [T, H] or null
+    uint16_t *norm_out;         // bf16 [T, H] or null
+    float routed_scale;
+    float eps;
+    int wkind;
+    int T, K, H;
+    int nvec;                   // vectors per row = H / vec
+    int splits;                 // CTAs per token
+    int slice;                  // vectors per CTA
+};
+
+// Launches one finalize according to `plan` (validated by the caller).
+cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan,
+                            cudaStream_t stream);
+
+cudaError_t launch_unpack(const int32_t *packed, int64_t n, int32_t *expert_ids,
+                          float *weights, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_check_indices(const int32_t *idx, int64_t n, int64_t P,
+                                 int32_t *d_bad_count, int num_sms, cudaStream_t stream);
+
+}  // namespace moef

@@ -1,0 +1,164 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the
+header declares, rejects bad arguments before touching CUDA, and plans
+launches as documented.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_deferred_finalize_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def mf():
+    build.build_library()
+    import moe_deferred_finalize_gb300 as m
+    return m
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^(?:const\s+)?\w+\s+\**\s*(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    assert {"moe_finalize", "moe_finalize_ex", "moe_finalize_plan", "unpack_topk_ids",
+            "moe_finalize_check_indices", "moef_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(mf):
+    lib = ctypes.CDLL(build.LIB)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(mf):
+    s = mf.lib().moef_status_string
+    for code in range(7):
+        assert s(code) and s(code) != b"unknown status"
+    assert s(99) == b"unknown status"
+
+
+# Argument errors are returned before any CUDA call, so they are checked here
+# with made-up (never dereferenced) addresses.
+A = 0x10000   # 64 KiB aligned fake addresses
+NULL = None
+
+
+def call(mf, **kw):
+    args = dict(x=A, P=16, idx=A, w=A, wkind=0, scale=1.0, shared=A, residual=NULL,
+                gamma=NULL, eps=1e-6, out=A, residual_out=NULL, norm_out=NULL, T=2, K=2, H=8,
+                stream=NULL)
+    args.update(kw)
+    return mf.lib().moe_finalize(args["x"], args["P"], args["idx"], args["w"], args["wkind"],
+                                 args["scale"], args["shared"], args["residual"], args["gamma"],
+                                 args["eps"], args["out"], args["residual_out"],
+                                 args["norm_out"], args["T"], args["K"], args["H"],
+                                 args["stream"])
+
+
+def test_argument_errors(mf):
+    OK, NUL, SHAPE, ALIGN, ARG = 0, 1, 2, 3, 4
+    assert call(mf, T=0) == OK                      # empty batch: nothing enqueued
+    assert call(mf, T=0, x=NULL) == OK
+    assert call(mf, T=-1) == SHAPE
+    assert call(mf, K=0) == SHAPE
+    assert call(mf, K=33) == SHAPE
+    assert call(mf, H=0) == SHAPE
+    assert call(mf, P=0) == SHAPE
+    assert call(mf, wkind=3) == ARG
+    assert call(mf, x=NULL) == NUL
+    assert call(mf, idx=NULL) == NUL
+    assert call(mf, w=NULL) == NUL
+    assert call(mf, shared=NULL) == NUL
+    assert call(mf, out=NULL) == NUL                # no residual: out is required
+    assert call(mf, residual=A) == ARG              # residual without gamma
+    assert call(mf, gamma=A) == ARG
+    assert call(mf, residual=A, gamma=A) == NUL     # residual_out / norm_out missing
+    assert call(mf, residual=A, gamma=A, residual_out=A) == NUL
+    assert call(mf, residual_out=A) == ARG          # output without its input
+    assert call(mf, residual=A, gamma=A, residual_out=A, norm_out=A, eps=-1.0) == ARG
+    assert call(mf, residual=A, gamma=A, residual_out=A, norm_out=A, eps=float("nan")) == ARG
+    assert call(mf, residual=A, gamma=A, residual_out=A, norm_out=A, eps=float("inf")) == ARG
+    assert call(mf, x=A + 1) == ALIGN
+    assert call(mf, out=A + 1) == ALIGN
+    assert call(mf, idx=A + 2) == ALIGN
+    assert call(mf, w=A + 2) == ALIGN               # fp32 weights need 4 bytes
+    u = mf.lib().unpack_topk_ids
+    assert u(A, 0, A, A, NULL) == OK
+    assert u(A, -1, A, A, NULL) == SHAPE
+    assert u(NULL, 4, A, A, NULL) == NUL
+    assert u(A, 4, NULL, NULL, NULL) == NUL
+    assert u(A + 2, 4, A, NULL, NULL) == ALIGN
+    c = mf.lib().moe_finalize_check_indices
+    assert c(A, 2, 2, 16, NULL, NULL) == NUL
+    assert c(A, -1, 2, 16, A, NULL) == SHAPE
+    assert c(A, 2, 0, 16, A, NULL) == SHAPE
+    assert c(NULL, 2, 2, 16, A, NULL) == NUL
+    assert c(A, 2, 2, 16, A + 2, NULL) == ALIGN
+
+
+def test_plan_regimes(mf):
+    # decode sizes: one 16-byte vector per thread, 128-vector slices
+    p = mf.plan(1, 8, 7168, False)
+    assert (p["vec"], p["splits"], p["slice"], p["threads"], p["vpt"], p["cluster"]) == \
+        (8, 7, 128, 128, 1, 1)
+    p = mf.plan(16, 8, 7168, True)
+    assert (p["splits"], p["cluster"], p["grid"]) == (7, 7, 112)
+    p = mf.plan(256, 8, 7168, False)
+    assert (p["splits"], p["vpt"], p["grid"]) == (7, 1, 1792)
+    # bandwidth sizes: one CTA of 128 threads per token row
+    p = mf.plan(16384, 8, 7168, True)
+    assert (p["splits"], p["threads"], p["vpt"], p["cluster"], p["grid"]) == (1, 128, 8, 1, 16384)
+    # scalar path when H is not a multiple of 8 or pointers are unaligned
+    assert mf.plan(4, 2, 100, False)["vec"] == 1
+    assert mf.plan(4, 2, 64, False, vec_ok=False)["vec"] == 1
+    # long RMSNorm rows use a cluster, up to 16 CTAs
+    p = mf.plan(4096, 8, 32768, True)
+    assert p["cluster"] == 2 and p["threads"] == 256 and p["vpt"] == 8
+    p = mf.plan(2, 8, 32768, True)
+    assert p["cluster"] == 16 and p["vpt"] == 1
+
+
+def test_plan_invariants(mf):
+    for T in (1, 3, 16, 256, 700, 5000, 16384):
+        for H in (8, 64, 100, 1000, 7168, 7176, 16384, 40000):
+            for norm in (False, True):
+                for vec_ok in (True, False):
+                    try:
+                        p = mf.plan(T, 8, H, norm, vec_ok)
+                    except mf.MoefError as e:
+                        assert e.status == 2 and norm     # only over-long norm rows fail
+                        continue
+                    nvec = H // p["vec"]
+                    assert p["vec"] in (1, 8) and (p["vec"] == 1 or H % 8 == 0)
+                    assert p["splits"] * p["slice"] >= nvec > (p["splits"] - 1) * p["slice"]
+                    assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 256
+                    assert p["vpt"] in (1, 2, 4, 8)
+                    assert p["grid"] == T * p["splits"]
+                    if norm:
+                        assert p["threads"] * p["vpt"] >= p["slice"]   # one pass per slice
+                        assert p["cluster"] == p["splits"] <= 16
+                    else:
+                        assert p["cluster"] == 1
+
+
+def test_plan_hints(mf):
+    p = mf.plan(1, 8, 7168, False, splits=28, threads=32)
+    assert (p["splits"], p["slice"], p["threads"], p["vpt"]) == (28, 32, 32, 1)
+    with pytest.raises(mf.MoefError):
+        mf.plan(1, 8, 7168, False, threads=48)
+    with pytest.raises(mf.MoefError):
+        mf.plan(1, 8, 7168, True, splits=17)
+    with pytest.raises(mf.MoefError):
+        mf.plan(1, 8, 7168, True, splits=1, threads=32)   # norm row needs 28 vectors/thread

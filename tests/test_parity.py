@@ -1,0 +1,239 @@
+"""CUDA path against the fp64 oracle, element by element, through the C ABI.
+
+Tolerance (every bf16 output): |gpu - oracle| <= 2^-7 |oracle| + 2e-3.
+Bit-exact where the arithmetic leaves no choice (one slot of weight 1,
+zero weights, identical tokens, launch shape changes for out/residual_out).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from moe_deferred_finalize_gb300 import workloads as W
+
+from gpu_util import (assert_close, bf16_dev, bits_of, compare, f64_of, run_gpu, run_oracle,
+                      to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_bs1_packed", "decode_bs256", "fused_norm_bs16"])
+def test_named_workloads(cuda_lib, orc, name):
+    wl = W.make(name)
+    ref = run_oracle(orc, wl)
+    compare(run_gpu(cuda_lib, wl), ref, f"{name}: ")
+    if wl.with_norm:
+        res = run_gpu(cuda_lib, wl, write_out=False)
+        assert res["out"] is None
+        compare(res, ref, f"{name} (no out): ")
+
+
+def test_norm_reproducible_from_residual_out(cuda_lib, orc):
+    """norm_out is the RMSNorm of the bf16 residual_out the kernel emitted."""
+    wl = W.make("fused_norm_bs16")
+    res = run_gpu(cuda_lib, wl)
+    ref = orc.rmsnorm_bf16(bits_of(res["residual_out"]), wl.gamma, wl.eps)
+    assert_close(f64_of(res["norm_out"]), ref, "norm_out vs own residual_out",
+                 rel=2.0 ** -8, abs_=1e-3)
+
+
+CASES = [
+    # (T, K, H, wkind, norm)
+    (1, 1, 8, "fp32", False),
+    (3, 2, 64, "bf16", True),
+    (5, 3, 100, "fp32", True),         # H % 8 != 0: scalar path
+    (7, 9, 136, "packed", False),      # K > 8: two slot groups
+    (2, 32, 264, "fp32", True),        # K at its maximum
+    (16, 8, 7168, "bf16", True),
+    (3, 8, 7176, "fp32", True),        # ragged: 897 vectors
+    (300, 8, 7168, "packed", False),
+    (300, 6, 1000, "fp32", True),
+    (700, 8, 7168, "fp32", True),      # just past the latency regime
+    (2, 4, 16384, "fp32", True),       # cluster of 16 CTAs
+    (40, 2, 24576, "fp32", True),      # bandwidth regime, norm row over 2 CTAs
+    (33, 5, 40000, "bf16", False),     # several passes per slice without norm
+    (9, 4, 4098, "fp32", True),        # H % 8 == 2: scalar path with cluster
+]
+
+
+@pytest.mark.parametrize("T,K,H,wkind,norm", CASES)
+def test_random_shapes(cuda_lib, orc, T, K, H, wkind, norm):
+    # about 8 rows per 32-row expert block: no block overflows in practice
+    tile = 32
+    n_blocks = max(K + 1, (T * K + 7) // 8)
+    wl = W.synth("case", T=T, K=K, H=H, E=2 * n_blocks + 64, tile=tile,
+                 P=n_blocks * tile, weight_rule="sigmoid", wkind=wkind,
+                 routed_scale=2.5, with_norm=norm, seed=T * 1000 + K * 10 + H, require_all=False)
+    compare(run_gpu(cuda_lib, wl), run_oracle(orc, wl), f"T={T} K={K} H={H} {wkind}: ")
+
+
+@pytest.mark.parametrize("splits,threads", [(1, 0), (1, 256), (2, 0), (3, 64), (7, 128),
+                                            (8, 0), (13, 96), (16, 0), (28, 32)])
+def test_launch_shapes_agree(cuda_lib, orc, splits, threads):
+    """Every legal launch shape gives the oracle's result; out and
+    residual_out are bit-identical across shapes (same per-element
+    arithmetic), norm_out agrees within tolerance."""
+    wl = W.make("fused_norm_bs16")
+    dev = to_device(wl)
+    base = run_gpu(cuda_lib, wl, dev)
+    res = run_gpu(cuda_lib, wl, dev, splits=splits, threads=threads)
+    compare(res, run_oracle(orc, wl), f"splits={splits} threads={threads}: ")
+    assert np.array_equal(bits_of(res["out"]), bits_of(base["out"]))
+    assert np.array_equal(bits_of(res["residual_out"]), bits_of(base["residual_out"]))
+
+
+def test_one_slot_weight_one_is_the_row(cuda_lib):
+    wl = W.synth("k1", T=9, K=1, H=7168, E=64, tile=16, P=256, seed=21)
+    dev = to_device(wl)
+    dev["w"] = torch.ones((9, 1), dtype=torch.float32, device="cuda")
+    dev["shared"] = torch.zeros((9, 7168), dtype=torch.bfloat16, device="cuda")
+    res = cuda_lib.moe_finalize(dev["x"], dev["idx"], dev["w"], "fp32", dev["shared"],
+                                routed_scale=1.0)
+    assert np.array_equal(bits_of(res["out"]), wl.permuted_out[wl.idx[:, 0]])
+
+
+def test_zero_weights_and_zero_scale_give_shared(cuda_lib):
+    wl = W.make("decode_bs256")
+    dev = to_device(wl)
+    res = cuda_lib.moe_finalize(dev["x"], dev["idx"], torch.zeros_like(dev["w"]), "fp32",
+                                dev["shared"], routed_scale=2.5)
+    assert np.array_equal(bits_of(res["out"]), wl.shared)
+    res = cuda_lib.moe_finalize(dev["x"], dev["idx"], dev["w"], "fp32", dev["shared"],
+                                routed_scale=0.0)
+    assert np.array_equal(bits_of(res["out"]), wl.shared)
+
+
+def test_slot_order_and_duplicates(cuda_lib, orc):
+    wl = W.make("fused_norm_bs16")
+    perm = np.random.default_rng(3).permutation(wl.K)
+    wl2 = W.Workload(**{**wl.__dict__, "idx": np.ascontiguousarray(wl.idx[:, perm]),
+                        "weights": np.ascontiguousarray(wl.weights[:, perm])})
+    compare(run_gpu(cuda_lib, wl2), run_oracle(orc, wl), "permuted slots: ")
+    # token 5 made identical to token 2: identical output rows, bit for bit
+    wl3 = W.Workload(**{**wl.__dict__})
+    for f in ("idx", "weights", "shared", "residual"):
+        a = getattr(wl, f).copy()
+        a[5] = a[2]
+        setattr(wl3, f, a)
+    res = run_gpu(cuda_lib, wl3)
+    for key in ("out", "residual_out", "norm_out"):
+        b = bits_of(res[key])
+        assert np.array_equal(b[5], b[2]), key
+
+
+def test_padding_never_read(cuda_lib):
+    wl = W.make("decode_bs256")
+    x = wl.permuted_out.copy()
+    x[~wl.valid_rows] = 0x7FC0      # NaN everywhere a row is not referenced
+    wl2 = W.Workload(**{**wl.__dict__, "permuted_out": x})
+    res = run_gpu(cuda_lib, wl2)
+    assert torch.isfinite(res["out"].float()).all()
+    wl = W.make("fused_norm_bs16")
+    x = wl.permuted_out.copy()
+    x[~wl.valid_rows] = 0x7FC0
+    res = run_gpu(cuda_lib, W.Workload(**{**wl.__dict__, "permuted_out": x}))
+    for key in ("out", "residual_out", "norm_out"):
+        assert torch.isfinite(res[key].float()).all(), key
+
+
+def test_in_place(cuda_lib):
+    wl = W.make("fused_norm_bs16")
+    dev = to_device(wl)
+    ref = run_gpu(cuda_lib, wl, dev)
+    sh, rs = dev["shared"].clone(), dev["residual"].clone()
+    cuda_lib.moe_finalize(dev["x"], dev["idx"], dev["w"], "fp32", sh, routed_scale=1.0,
+                          residual=rs, gamma=dev["gamma"], eps=wl.eps, out=sh, residual_out=rs)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(sh), bits_of(ref["out"]))
+    assert np.array_equal(bits_of(rs), bits_of(ref["residual_out"]))
+
+
+def test_unaligned_pointers_take_scalar_path(cuda_lib, orc):
+    """Operands at a 2-byte offset (not 16-byte aligned) give the same result."""
+    wl = W.make("fused_norm_bs16")
+    ref = run_oracle(orc, wl)
+    T, H = wl.T, wl.H
+
+    def shifted(bits):
+        flat = np.zeros(bits.size + 1, np.uint16)
+        flat[1:] = bits.ravel()
+        return bf16_dev(flat)[1:].view(bits.shape)
+
+    dev = to_device(wl)
+    x = shifted(wl.permuted_out)
+    sh, rs, g = shifted(wl.shared), shifted(wl.residual), shifted(wl.gamma)
+    outs = [torch.empty(T * H + 1, dtype=torch.bfloat16, device="cuda")[1:].view(T, H)
+            for _ in range(3)]
+    assert x.data_ptr() % 16 == 2
+    res = cuda_lib.moe_finalize(x, dev["idx"], dev["w"], "fp32", sh, routed_scale=1.0,
+                                residual=rs, gamma=g, eps=wl.eps, out=outs[0],
+                                residual_out=outs[1], norm_out=outs[2])
+    torch.cuda.synchronize()
+    compare(res, ref, "unaligned: ")
+    base = run_gpu(cuda_lib, wl, dev)
+    assert np.array_equal(bits_of(res["out"]), bits_of(base["out"]))
+
+
+def test_empty_batch(cuda_lib):
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    idx = torch.zeros((0, 2), dtype=torch.int32, device="cuda")
+    w = torch.zeros((0, 2), dtype=torch.float32, device="cuda")
+    sh = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    res = cuda_lib.moe_finalize(x, idx, w, "fp32", sh)
+    assert res["out"].shape == (0, 64)
+
+
+def test_fp32_weights_read_as_bf16_fail_parity(cuda_lib, orc):
+    """The failure of "[Deepseek V4] Keep fp32 routing weights in the mxfp4
+    trtllm MoE" (revert note): fp32 weight buffers reinterpreted as bf16.
+    The parity check must see it."""
+    wl = W.make("decode_bs256")
+    dev = to_device(wl)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    lib = cuda_lib.lib()
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = lib.moe_finalize(p(dev["x"]), wl.P, p(dev["idx"]), p(dev["w"]), 1, 2.5,
+                          p(dev["shared"]), None, None, 0.0, p(out), None, None,
+                          wl.T, wl.K, wl.H, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    with pytest.raises(AssertionError):
+        assert_close(f64_of(out), run_oracle(orc, wl)["out"], "misread weights")
+
+
+def test_graph_capture_replay(cuda_lib, orc):
+    wl = W.make("fused_norm_bs16")
+    dev = to_device(wl)
+    outs = {k: torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+            for k in ("out", "residual_out", "norm_out")}
+
+    def step():
+        cuda_lib.moe_finalize(dev["x"], dev["idx"], dev["w"], "fp32", dev["shared"],
+                              routed_scale=1.0, residual=dev["residual"], gamma=dev["gamma"],
+                              eps=wl.eps, **outs)
+
+    step()                      # first call outside capture
+    torch.cuda.synchronize()
+    for t in outs.values():
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    compare(outs, run_oracle(orc, wl), "graph replay: ")
+
+
+def test_error_statuses_on_device(cuda_lib):
+    wl = W.make("tiny")
+    dev = to_device(wl)
+    with pytest.raises(cuda_lib.MoefError) as e:
+        cuda_lib.moe_finalize(dev["x"], dev["idx"], dev["w"], "fp32", dev["shared"],
+                              splits=40, threads=48)
+    assert e.value.status == 4
+    with pytest.raises(ValueError):
+        cuda_lib.moe_finalize(dev["x"], dev["idx"], dev["w"].double(), "fp32", dev["shared"])
