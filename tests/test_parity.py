@@ -69,7 +69,7 @@ def test_random_shapes(cuda_lib, orc, T, K, H, wkind, norm):
 
 
 @pytest.mark.parametrize("splits,threads", [(1, 0), (1, 256), (2, 0), (3, 64), (7, 128),
-                                            (8, 0), (13, 96), (16, 0), (28, 32)])
+                                            (8, 0), (13, 96), (16, 0)])
 def test_launch_shapes_agree(cuda_lib, orc, splits, threads):
     """Every legal launch shape gives the oracle's result; out and
     residual_out are bit-identical across shapes (same per-element
@@ -81,6 +81,26 @@ def test_launch_shapes_agree(cuda_lib, orc, splits, threads):
     compare(res, run_oracle(orc, wl), f"splits={splits} threads={threads}: ")
     assert np.array_equal(bits_of(res["out"]), bits_of(base["out"]))
     assert np.array_equal(bits_of(res["residual_out"]), bits_of(base["residual_out"]))
+
+
+@pytest.mark.parametrize("splits,threads", [(1, 0), (1, 32), (4, 64), (28, 32), (56, 0),
+                                            (112, 32), (896, 32)])
+def test_launch_shapes_agree_without_norm(cuda_lib, orc, splits, threads):
+    """Without RMSNorm a row may be cut into any number of slices."""
+    wl = W.make("decode_bs256")
+    dev = to_device(wl)
+    base = run_gpu(cuda_lib, wl, dev)
+    res = run_gpu(cuda_lib, wl, dev, splits=splits, threads=threads)
+    compare(res, run_oracle(orc, wl), f"splits={splits} threads={threads}: ")
+    assert np.array_equal(bits_of(res["out"]), bits_of(base["out"]))
+
+
+def test_norm_split_beyond_cluster_limit_is_rejected(cuda_lib):
+    wl = W.make("fused_norm_bs16")
+    dev = to_device(wl)
+    with pytest.raises(cuda_lib.MoefError) as e:
+        run_gpu(cuda_lib, wl, dev, splits=17)
+    assert e.value.status == 4
 
 
 def test_one_slot_weight_one_is_the_row(cuda_lib):
