@@ -1,0 +1,48 @@
+"""Run the finalize on one synthetic configuration a few times (no checks).
+
+For profilers: one process, a handful of launches, a known input size.
+
+  python -m moe_deferred_finalize_gb300.run_case --workload decode_bs256 --iters 3
+  python -m moe_deferred_finalize_gb300.run_case --prefill-tokens 4096 --iters 3
+"""
+import argparse
+
+import numpy as np
+import torch
+
+import moe_deferred_finalize_gb300 as mf
+from moe_deferred_finalize_gb300 import workloads as W
+
+
+def _dev(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    g = ap.add_mutually_exclusive_group(required=True)
+    g.add_argument("--workload", choices=W.CONFIG_NAMES)
+    g.add_argument("--prefill-tokens", type=int)
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--write-out", action="store_true",
+                    help="with a residual, also write out (default: residual_out + norm_out only)")
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--threads", type=int, default=0)
+    args = ap.parse_args(argv)
+    wl = W.make(args.workload) if args.workload else W.prefill(args.prefill_tokens)
+    x, idx, w, sh = _dev(wl.permuted_out), _dev(wl.idx), _dev(wl.weights), _dev(wl.shared)
+    res = _dev(wl.residual) if wl.with_norm else None
+    gam = _dev(wl.gamma) if wl.with_norm else None
+    for _ in range(args.iters):
+        mf.moe_finalize(x, idx, w, wl.wkind, sh, routed_scale=wl.routed_scale, residual=res,
+                        gamma=gam, eps=wl.eps, write_out=args.write_out or not wl.with_norm,
+                        splits=args.splits, threads=args.threads)
+    torch.cuda.synchronize()
+    print(f"{wl.name}: T={wl.T} K={wl.K} H={wl.H} P={wl.P} iters={args.iters} ok")
+
+
+if __name__ == "__main__":
+    main()

@@ -274,16 +274,33 @@ def synth(name: str, T: int, K: int, H: int, E: int, tile: int, *,
 # ------------------------------------------------------ the five workloads
 
 
-def c5_counts(seed_seq: np.random.SeedSequence, E: int = 256) -> np.ndarray:
-    """Load-balanced exact counts for 16384 tokens x top-8 over 256 experts:
-    16 experts take 544 slots, 16 take 480 and 224 take 512 (131072 slots,
-    1040 tiles of 128 rows = 133120 permuted rows)."""
+def balanced_counts(T: int, K: int, E: int, seed_seq: np.random.SeedSequence) -> np.ndarray:
+    """Load-balanced exact counts for T tokens x top-K over E experts: with
+    base = T*K/E, 16 experts take base + base/16 slots, 16 take base - base/16
+    and the rest take base (T*K must be a multiple of 16*E).  For 16384
+    tokens x top-8 over 256 experts that is 16 x 544, 16 x 480, 224 x 512
+    slots: 131072 slots in 1040 tiles of 128 rows = 133120 permuted rows."""
+    if (T * K) % (16 * E):
+        raise ValueError("T*K must be a multiple of 16*E")
+    base = T * K // E
+    delta = base // 16
     rng = np.random.Generator(np.random.PCG64(seed_seq))
-    counts = np.full(E, 512, np.int64)
+    counts = np.full(E, base, np.int64)
     who = rng.permutation(E)
-    counts[who[:16]] = 544
-    counts[who[16:32]] = 480
+    counts[who[:16]] = base + delta
+    counts[who[16:32]] = base - delta
     return counts
+
+
+def prefill(T: int, alloc: Alloc = _np_alloc, threads: Optional[int] = None,
+            name: Optional[str] = None) -> Workload:
+    """Prefill-shaped workload with T tokens: K=8 of E=256 experts with
+    balanced exact counts, blocks padded to 128 rows, H=7168, fp32
+    normalised-sigmoid routing, routed scale 2.5, residual + RMSNorm."""
+    counts = balanced_counts(T, 8, 256, np.random.SeedSequence([4, 1]))
+    return synth(name or f"prefill_t{T}", T=T, K=8, H=7168, E=256, tile=128,
+                 counts_per_expert=counts, weight_rule="sigmoid", routed_scale=2.5,
+                 with_norm=True, eps=1e-6, seed=4, alloc=alloc, threads=threads)
 
 
 CONFIG_NAMES = ("tiny", "decode_bs1_packed", "decode_bs256",
@@ -308,8 +325,5 @@ def make(name: str, alloc: Alloc = _np_alloc, threads: Optional[int] = None) -> 
                      routed_scale=1.0, with_norm=True, eps=1e-6, seed=3, alloc=alloc,
                      threads=threads)
     if name == "prefill_t16384":
-        counts = c5_counts(np.random.SeedSequence([4, 1]))
-        return synth(name, T=16384, K=8, H=7168, E=256, tile=128, counts_per_expert=counts,
-                     weight_rule="sigmoid", routed_scale=2.5, with_norm=True, eps=1e-6,
-                     seed=4, alloc=alloc, threads=threads)
+        return prefill(16384, alloc=alloc, threads=threads, name=name)
     raise KeyError(name)

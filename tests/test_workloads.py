@@ -57,7 +57,7 @@ def test_deterministic():
 
 
 def test_prefill_exact_counts_routing():
-    counts = W.c5_counts(np.random.SeedSequence([4, 1]))
+    counts = W.balanced_counts(16384, 8, 256, np.random.SeedSequence([4, 1]))
     assert counts.sum() == 16384 * 8
     assert int((((counts + 127) // 128) * 128).sum()) == 133120
     rng = np.random.Generator(np.random.PCG64(0))
@@ -73,3 +73,9 @@ def test_small_random_layout():
                  wkind="bf16", seed=9, with_norm=True)
     _check_layout(wl)
     assert wl.weights.dtype == np.uint16 and wl.gamma.shape == (24,)
+
+
+def test_prefill_scaled_counts():
+    counts = W.balanced_counts(4096, 8, 256, np.random.SeedSequence([4, 1]))
+    assert sorted(set(counts.tolist())) == [120, 128, 136]
+    assert int((((counts + 127) // 128) * 128).sum()) == 34816
