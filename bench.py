@@ -235,22 +235,33 @@ def decode_latency(mf, name, device, reps):
     outs = torch.empty((R, wl.T, wl.H), dtype=torch.bfloat16, device=device)
     sets = [({"x": xs[r], "idx": d["idx"], "w": d["w"], "shared": shs[r]}, {"out": outs[r]})
             for r in range(R)]
+    bound = [mf.bind(dd["x"], dd["idx"], dd["w"], wl.wkind, dd["shared"],
+                     routed_scale=wl.routed_scale, out=oo["out"]) for dd, oo in sets]
 
     def one_pass():
         for dd, oo in sets:
             call(mf, wl, dd, oo)
 
+    def one_pass_bound():
+        for f in bound:
+            f()
+
     one_pass()
+    one_pass_bound()
     torch.cuda.synchronize(device)
-    # eager, back to back
     n_pass = max(1, reps // R)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n_pass):
-        one_pass()
-    b.record()
-    torch.cuda.synchronize(device)
-    eager_us = a.elapsed_time(b) * 1e3 / (n_pass * R)
+
+    def eager(fn):
+        a.record()
+        for _ in range(n_pass):
+            fn()
+        b.record()
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) * 1e3 / (n_pass * R)
+
+    eager_checked_us = eager(one_pass)      # argument checks on every call
+    eager_us = eager(one_pass_bound)        # checked once, then raw C-ABI calls
     # CUDA graph of one pass over all copies, replayed
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream(device)
@@ -272,9 +283,10 @@ def decode_latency(mf, name, device, reps):
     graph_us = statistics.median(samples)
     plan = mf.plan(wl.T, wl.K, wl.H, False, True,
                    torch.cuda.get_device_properties(device).multi_processor_count)
-    del xs, shs, outs, g
+    del xs, shs, outs, g, bound
     return {"T": wl.T, "K": wl.K, "H": wl.H, "routing": wl.wkind,
             "us_per_call_graph": round(graph_us, 3), "us_per_call_eager": round(eager_us, 3),
+            "us_per_call_eager_checked": round(eager_checked_us, 3),
             "GBps_graph": round(touched / (graph_us * 1e-6) / 1e9, 1),
             "copies": R, "calls": n_pass * R, "plan": plan}
 

@@ -7,8 +7,8 @@ the residual followed by RMSNorm, in one CUDA kernel for sm_103a.  The
 kernels and their C ABI live in ``libmoe_finalize.so``
 (``include/moe_finalize.h``); this package is its thin Python binding.
 """
-from ._abi import (WKIND, MoefError, check_indices, lib, moe_finalize, plan,  # noqa: F401
-                   unpack_topk_ids)
+from ._abi import (WKIND, BoundFinalize, MoefError, bind, check_indices, lib,  # noqa: F401
+                   moe_finalize, plan, unpack_topk_ids)
 
-__all__ = ["moe_finalize", "unpack_topk_ids", "check_indices", "plan", "lib", "MoefError",
-           "WKIND"]
+__all__ = ["moe_finalize", "bind", "BoundFinalize", "unpack_topk_ids", "check_indices", "plan",
+           "lib", "MoefError", "WKIND"]

@@ -83,6 +83,8 @@ def _ptr(t: Optional[torch.Tensor]):
 def _stream(stream, device):
     if stream is None:
         return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if isinstance(stream, ctypes.c_void_p):
+        return stream
     if isinstance(stream, torch.cuda.Stream):
         return ctypes.c_void_p(stream.cuda_stream)
     return ctypes.c_void_p(int(stream))
@@ -104,23 +106,9 @@ def _check(t, name, dtypes, shape, device):
 _BF16 = (torch.bfloat16,)
 
 
-def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: torch.Tensor,
-                 wkind: str, shared_out: torch.Tensor, *, routed_scale: float = 1.0,
-                 residual: Optional[torch.Tensor] = None, gamma: Optional[torch.Tensor] = None,
-                 eps: float = 1e-6, out: Optional[torch.Tensor] = None,
-                 residual_out: Optional[torch.Tensor] = None,
-                 norm_out: Optional[torch.Tensor] = None, write_out: bool = True,
-                 splits: int = 0, threads: int = 0, stream=None) -> dict:
-    """Deferred MoE finalize on the GPU (see include/moe_finalize.h).
-
-    permuted_out bf16 [P, H]; idx_map int32 [T, K]; weights [T, K] encoded
-    as ``wkind`` ("fp32": float32, "bf16": bfloat16, "packed": int32 words
-    (expert_id << 16) | bf16(weight)); shared_out bf16 [T, H]; optional
-    residual bf16 [T, H] with gamma bf16 [H].  Outputs are allocated when not
-    given; with a residual, ``write_out=False`` skips ``out``.  Returns a dict
-    with "out" and, with a residual, "residual_out" and "norm_out".
-    Enqueued on the current stream (or ``stream``); nothing is synchronised.
-    """
+def _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale, residual, gamma,
+             eps, out, residual_out, norm_out, write_out, splits, threads):
+    """Validate, allocate missing outputs; returns (C arguments, outputs)."""
     if wkind not in WKIND:
         raise ValueError(f"wkind must be one of {sorted(WKIND)}")
     device = permuted_out.device
@@ -154,19 +142,78 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
         _check(out, "out", _BF16, (T, H), device)
     else:
         out = None
-
-    st = _lib().moe_finalize_ex(
-        _ptr(permuted_out), P, _ptr(idx_map), _ptr(weights), WKIND[wkind],
-        float(routed_scale), _ptr(shared_out), _ptr(residual), _ptr(gamma), float(eps),
-        _ptr(out), _ptr(residual_out), _ptr(norm_out), T, K, H, int(splits), int(threads),
-        _stream(stream, device))
-    if st != 0:
-        raise MoefError(st, "moe_finalize")
+    args = (_ptr(permuted_out), P, _ptr(idx_map), _ptr(weights), WKIND[wkind],
+            float(routed_scale), _ptr(shared_out), _ptr(residual), _ptr(gamma), float(eps),
+            _ptr(out), _ptr(residual_out), _ptr(norm_out), T, K, H, int(splits), int(threads))
     res = {"out": out}
     if norm:
         res["residual_out"] = residual_out
         res["norm_out"] = norm_out
+    return args, res
+
+
+def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: torch.Tensor,
+                 wkind: str, shared_out: torch.Tensor, *, routed_scale: float = 1.0,
+                 residual: Optional[torch.Tensor] = None, gamma: Optional[torch.Tensor] = None,
+                 eps: float = 1e-6, out: Optional[torch.Tensor] = None,
+                 residual_out: Optional[torch.Tensor] = None,
+                 norm_out: Optional[torch.Tensor] = None, write_out: bool = True,
+                 splits: int = 0, threads: int = 0, stream=None) -> dict:
+    """Deferred MoE finalize on the GPU (see include/moe_finalize.h).
+
+    permuted_out bf16 [P, H]; idx_map int32 [T, K]; weights [T, K] encoded
+    as ``wkind`` ("fp32": float32, "bf16": bfloat16, "packed": int32 words
+    (expert_id << 16) | bf16(weight)); shared_out bf16 [T, H]; optional
+    residual bf16 [T, H] with gamma bf16 [H].  Outputs are allocated when not
+    given; with a residual, ``write_out=False`` skips ``out``.  Returns a dict
+    with "out" and, with a residual, "residual_out" and "norm_out".
+    Enqueued on the current stream (or ``stream``); nothing is synchronised.
+    """
+    args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
+                         residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
+                         threads)
+    st = _lib().moe_finalize_ex(*args, _stream(stream, permuted_out.device))
+    if st != 0:
+        raise MoefError(st, "moe_finalize")
     return res
+
+
+class BoundFinalize:
+    """A finalize whose arguments were checked and marshalled once.
+
+    Calling it enqueues the same finalize again (same buffers, new contents
+    allowed) with no per-call Python checks: the decode-loop form of
+    ``moe_finalize``.  The tensors passed to ``bind`` must stay alive and
+    keep their storage while the object is used.
+    """
+
+    def __init__(self, args, res, stream, device):
+        self._fn = _lib().moe_finalize_ex
+        self._args = args
+        self._stream = _stream(stream, device)
+        self.outputs = res
+
+    def __call__(self, stream=None):
+        st = self._fn(*self._args, self._stream if stream is None else _stream(stream, None))
+        if st != 0:
+            raise MoefError(st, "moe_finalize")
+        return self.outputs
+
+
+def bind(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: torch.Tensor, wkind: str,
+         shared_out: torch.Tensor, *, routed_scale: float = 1.0,
+         residual: Optional[torch.Tensor] = None, gamma: Optional[torch.Tensor] = None,
+         eps: float = 1e-6, out: Optional[torch.Tensor] = None,
+         residual_out: Optional[torch.Tensor] = None, norm_out: Optional[torch.Tensor] = None,
+         write_out: bool = True, splits: int = 0, threads: int = 0,
+         stream=None) -> BoundFinalize:
+    """Check and marshal a finalize once (arguments as for ``moe_finalize``);
+    the returned object enqueues it on ``stream`` (default: the current
+    stream at bind time) each time it is called."""
+    args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
+                         residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
+                         threads)
+    return BoundFinalize(args, res, stream, permuted_out.device)
 
 
 def plan(T: int, K: int, H: int, with_norm: bool, vec_ok: bool = True, num_sms: int = 152,
