@@ -18,8 +18,11 @@
 // gathered byte is read exactly once), plus the shared and residual loads,
 // and accumulates in fp32 registers.  Outputs are written with streaming
 // stores.  The token's row indices and scaled weights are staged once in
-// shared memory.  With RMSNorm the bf16-rounded residual_out vectors stay in
-// registers between the two passes; the sum of squares is reduced with warp
+// shared memory.  With RMSNorm the bf16-rounded residual_out vectors are kept
+// in shared memory between the two passes (each thread its own column, so
+// no barrier is needed; in registers they cost 32 registers per thread and
+// halved the resident CTAs, and with them the loads in flight); the sum of
+// squares is reduced with warp
 // shuffles and shared memory, and across the CTAs of a split row through
 // distributed shared memory of a thread-block cluster (every CTA adds the
 // partials in the same order, so all slices use the same inverse RMS).
@@ -136,6 +139,10 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
     __shared__ float s_w[MOEF_MAX_K];
     __shared__ float s_warp[kMaxThreads / 32];
     __shared__ float s_cta;
+    // With RMSNorm: the bf16 residual_out vectors of this CTA's slice, kept
+    // for the second pass ([VPT][blockDim.x], each thread its own column).
+    extern __shared__ __align__(16) unsigned char s_dyn[];
+    V *s_keep = reinterpret_cast<V *>(s_dyn);
 
     const int S = p.splits;
     const int t = blockIdx.x / S;
@@ -159,7 +166,6 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
     const int v_end = min(v_begin + p.slice, p.nvec);
 
     float ss = 0.f;
-    V keep[NORM ? VPT : 1];
 
     for (int base = v_begin; base < v_end; base += nt * VPT) {
 #pragma unroll
@@ -201,7 +207,7 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
                     for (int q = 0; q < VEC; ++q) acc[q] += f[q];
                     const V sv = Ops::from_f32(acc);
                     Ops::store(p.residual_out + tok + e, sv);
-                    keep[j] = sv;
+                    s_keep[j * nt + threadIdx.x] = sv;
                     Ops::to_f32(sv, f);
 #pragma unroll
                     for (int q = 0; q < VEC; ++q) ss = fmaf(f[q], f[q], ss);
@@ -244,7 +250,7 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
             const int v = v_begin + threadIdx.x + j * nt;
             if (v < v_end) {
                 float sf[VEC], gf[VEC];
-                Ops::to_f32(keep[j], sf);
+                Ops::to_f32(s_keep[j * nt + threadIdx.x], sf);
                 Ops::to_f32(g[j], gf);
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) sf[q] = sf[q] * inv * gf[q];
@@ -283,7 +289,8 @@ cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, cudaStream_
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
     cfg.blockDim = dim3(static_cast<unsigned>(plan.threads));
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes =
+        NORM ? static_cast<size_t>(plan.threads) * VPT * sizeof(typename VecOps<VEC>::V) : 0;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = num_attrs;
