@@ -116,6 +116,13 @@ typedef enum {
  * is used when H % 8 == 0 and every bf16 pointer is 16-byte aligned; any
  * other case takes a scalar path with the same results.
  *
+ * Ordering: the kernel is launched as a programmatic dependent of the
+ * previous kernel on `stream` (programmatic stream serialization).  It
+ * touches no global memory before the previous kernel has completed and
+ * flushed, so ordinary stream order holds; only the launch and CTA set-up
+ * overlap the previous kernel's tail.  After its loads it allows the next
+ * kernel, if that one is launched the same way, to begin launching.
+ *
  * The call allocates nothing and does not synchronise, so it may be
  * captured in a CUDA graph ("[Kimi K2.5] Fuse deferred MoE finalize ...",
  * Key modifications: workspace sized before capture, never grown inside

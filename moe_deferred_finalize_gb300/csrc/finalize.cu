@@ -150,6 +150,25 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
     const int K = p.K;
     const int nt = blockDim.x;
 
+    const int64_t tok = static_cast<int64_t>(t) * p.H;
+    const int v_begin = split * p.slice;
+    const int v_end = min(v_begin + p.slice, p.nvec);
+
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: nothing before this point touches global memory, so the launch
+    // and CTA set-up overlap the previous kernel's tail, and every read and
+    // write below sees it complete.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // This thread's first dense operands do not depend on the row map: their
+    // loads go out before the staging barrier, beside the row-map loads.
+    const int v_first = v_begin + threadIdx.x;
+    V sh_first, rs_first;
+    if (v_first < v_end) {
+        sh_first = Ops::load(p.shared + tok + static_cast<int64_t>(v_first) * VEC);
+        if (NORM) rs_first = Ops::load(p.residual + tok + static_cast<int64_t>(v_first) * VEC);
+    }
+
     // Stage the token's row pointers and scaled weights (the routed scale
     // folded into the weight once, "Support deferred MoE finalize ...",
     // Modifications item 2).
@@ -161,10 +180,6 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
     }
     __syncthreads();
 
-    const int64_t tok = static_cast<int64_t>(t) * p.H;
-    const int v_begin = split * p.slice;
-    const int v_end = min(v_begin + p.slice, p.nvec);
-
     float ss = 0.f;
 
     for (int base = v_begin; base < v_end; base += nt * VPT) {
@@ -173,9 +188,10 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
             const int v = base + threadIdx.x + j * nt;
             if (v < v_end) {
                 const int64_t e = static_cast<int64_t>(v) * VEC;
-                const V sh = Ops::load(p.shared + tok + e);
+                const bool first = (j == 0) && (base == v_begin);
+                const V sh = first ? sh_first : Ops::load(p.shared + tok + e);
                 V rs;
-                if (NORM) rs = Ops::load(p.residual + tok + e);
+                if (NORM) rs = first ? rs_first : Ops::load(p.residual + tok + e);
 
                 float acc[VEC];
 #pragma unroll
@@ -216,6 +232,9 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
         }
         if (NORM) break;   // the plan gives a norm row slice one pass
     }
+    // All gathered loads of this CTA are done: the next kernel on the stream
+    // may begin launching (it waits for this grid before touching memory).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if constexpr (NORM) {
         // gamma loads go out before the reductions so their latency overlaps
@@ -264,8 +283,11 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
 template <int VPT, int VEC, bool NORM, bool CLUSTER>
 cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, cudaStream_t stream) {
     auto kern = finalize_kernel<VPT, VEC, NORM, CLUSTER>;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     unsigned num_attrs = 0;
+    attr[num_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[num_attrs].val.programmaticStreamSerializationAllowed = 1;
+    ++num_attrs;
     if (CLUSTER) {
         if (plan.cluster > 8) {
             // Clusters of 9..16 CTAs are opt-in per kernel and device.
@@ -280,11 +302,11 @@ cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, cudaStream_
                 enabled[dev] = 1;
             }
         }
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(plan.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        num_attrs = 1;
+        attr[num_attrs].id = cudaLaunchAttributeClusterDimension;
+        attr[num_attrs].val.clusterDim.x = static_cast<unsigned>(plan.cluster);
+        attr[num_attrs].val.clusterDim.y = 1;
+        attr[num_attrs].val.clusterDim.z = 1;
+        ++num_attrs;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
