@@ -64,16 +64,23 @@ const char *moef_status_string(moef_status s) {
     return "unknown status";
 }
 
-// Plan choice.  Two regimes:
-//  * latency: while one 16-byte vector per thread fits in about two waves of
-//    fully occupied SMs, every thread takes one vector (vpt = 1) and a row
-//    is cut into 128-vector slices, one CTA each.  This puts every gathered
-//    load of the call in flight at once, which is what decode batch sizes
-//    need (the time is a few memory latencies, not bytes).
-//  * bandwidth: otherwise one CTA of 128 (or 256) threads owns a whole row,
-//    each thread several vectors, and the grid has one CTA per token.
-// With RMSNorm a row must fit one pass of one CTA (at most 256 x 8
-// vectors), or one cluster of at most 16 CTAs.
+// Plan choice, from sweeps of T = 1..4096 at H = 7168 on GB300 (graph
+// replay, inputs larger than L2):
+//  * without RMSNorm, latency regime: while one 16-byte vector per thread
+//    fits in about two waves of fully occupied SMs, every thread takes one
+//    vector (vpt = 1) and a row is cut into 128-vector slices, one CTA each.
+//    Every gathered load of the call is then in flight at once, which is
+//    what decode batch sizes need (the time is a few memory latencies).
+//  * without RMSNorm, bandwidth regime: one CTA of 128 threads per token
+//    row, each thread up to 8 vectors.
+//  * with RMSNorm a row must be finished by one CTA or one cluster, and
+//    cluster launches cost more the larger and the more numerous they are:
+//    rows are split into slices of at most 256 vectors (one per thread of a
+//    256-thread CTA) only while the grid stays under about 3 CTAs per SM;
+//    from there on one CTA takes a whole row (256 threads below 4 rows per
+//    SM, then 128).  At T = 512 this is 1.5x faster than 7-CTA clusters.
+// A row with RMSNorm must fit one pass of one CTA (256 x 8 vectors) or one
+// cluster of at most 16 such CTAs.
 moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, int num_sms,
                               int splits_hint, int threads_hint, moef_plan *plan) {
     if (!plan) return MOEF_ERR_NULL;
@@ -83,17 +90,24 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, in
 
     const int vec = (vec_ok && H % 8 == 0) ? 8 : 1;
     const int nvec = H / vec;
+    const int64_t rows = T > 0 ? T : 1;
 
     int splits;
+    int threads_auto = 0;
     if (splits_hint) {
         splits = splits_hint < nvec ? splits_hint : nvec;
+    } else if (with_norm) {
+        const int row_fit = ceil_div(nvec, kMaxThreads * kMaxVpt);
+        splits = ceil_div(nvec, kMaxThreads);
+        const int by_grid = ceil_div(3 * static_cast<int64_t>(num_sms), rows);
+        if (splits > by_grid) splits = by_grid;
+        if (splits < row_fit) splits = row_fit;
+        if (splits > kMaxCluster) splits = kMaxCluster;
+        if (splits == 1) threads_auto = rows < 4 * static_cast<int64_t>(num_sms) ? kMaxThreads : 128;
     } else {
-        const int64_t one_per_thread = static_cast<int64_t>(T) * nvec;
+        const int64_t one_per_thread = rows * nvec;
         const int64_t two_waves = static_cast<int64_t>(num_sms) * 2048 * 2;
         splits = (one_per_thread <= two_waves) ? ceil_div(nvec, 128) : 1;
-        if (!threads_hint && splits == 1 && with_norm && nvec > kMaxThreads * kMaxVpt)
-            splits = ceil_div(nvec, kMaxThreads * kMaxVpt);
-        if (with_norm && splits > kMaxCluster) splits = kMaxCluster;
     }
     if (with_norm && splits > kMaxCluster) return MOEF_ERR_ARG;
 
@@ -103,6 +117,9 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, in
     int threads;
     if (threads_hint) {
         threads = threads_hint;
+    } else if (threads_auto && splits == 1) {
+        threads = threads_auto;
+        if (ceil_div(slice, threads) > kMaxVpt) threads = kMaxThreads;
     } else {
         const int cap = splits > 1 ? kMaxThreads : 128;
         threads = round_up(slice < cap ? slice : cap, 32);

@@ -113,8 +113,12 @@ def test_plan_regimes(mf):
     p = mf.plan(1, 8, 7168, False)
     assert (p["vec"], p["splits"], p["slice"], p["threads"], p["vpt"], p["cluster"]) == \
         (8, 7, 128, 128, 1, 1)
-    p = mf.plan(16, 8, 7168, True)
-    assert (p["splits"], p["cluster"], p["grid"]) == (7, 7, 112)
+    p = mf.plan(16, 8, 7168, True)          # RMSNorm: 4-CTA clusters, one vector per thread
+    assert (p["splits"], p["threads"], p["vpt"], p["cluster"], p["grid"]) == (4, 224, 1, 4, 64)
+    p = mf.plan(256, 8, 7168, True)
+    assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (2, 256, 2, 2)
+    p = mf.plan(512, 8, 7168, True)         # one CTA per row from ~3 CTAs per SM on
+    assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (1, 256, 4, 1)
     p = mf.plan(256, 8, 7168, False)
     assert (p["splits"], p["vpt"], p["grid"]) == (7, 1, 1792)
     # bandwidth sizes: one CTA of 128 threads per token row
@@ -126,6 +130,8 @@ def test_plan_regimes(mf):
     # long RMSNorm rows use a cluster, up to 16 CTAs
     p = mf.plan(4096, 8, 32768, True)
     assert p["cluster"] == 2 and p["threads"] == 256 and p["vpt"] == 8
+    p = mf.plan(8, 8, 16384, True)
+    assert p["cluster"] == 8 and p["threads"] == 256 and p["vpt"] == 1
     p = mf.plan(2, 8, 32768, True)
     assert p["cluster"] == 16 and p["vpt"] == 1
 
