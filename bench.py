@@ -350,9 +350,10 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return 0
     wl = W.make(WORKLOAD)
-    # per step a token sample sized so that all steps take about a minute
+    # per step a token sample sized so that all steps take about ref_budget_s
     per_token_s = 4e-4
-    n_tok = int(np.clip(60.0 / max(1, args.steps + args.warmup) / per_token_s, 8, wl.T))
+    n_tok = int(np.clip(args.ref_budget_s / max(1, args.steps + args.warmup) / per_token_s,
+                        8, wl.T))
     starts = [(i * n_tok) % (wl.T - n_tok + 1) for i in range(args.steps + args.warmup)]
     times = []
     for i, s0 in enumerate(starts):
@@ -465,6 +466,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-decode", action="store_true", help="omit the decode latency lines")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU oracle baseline")
+    ap.add_argument("--ref-budget-s", type=float, default=60.0,
+                    help="--impl reference: seconds of oracle work over all steps")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
