@@ -46,7 +46,8 @@ WORKLOAD = "prefill_t16384"
 METRIC = "finalize µs/call at T=1,256; HBM GB/s (% of peak) at T=16384, H=7168"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "moe_deferred_finalize_gb300", "csrc", "finalize.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "moe_deferred_finalize_gb300", "csrc", f)
+               for f in ("finalize.cu", "vec.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
 
@@ -111,7 +112,10 @@ def recorded_traffic():
         return None
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
-    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    h = hashlib.sha256()
+    for f in KERNEL_SRCS:
+        h.update(open(f, "rb").read())
+    sha = h.hexdigest()
     if d.get("kernel_src_sha256") != sha or d.get("workload") != WORKLOAD:
         return None
     return d.get("dram_bytes_per_launch")
@@ -226,17 +230,28 @@ def decode_latency(mf, name, device, reps):
     """µs per call on inputs rotated through copies whose total exceeds L2."""
     wl = W.make(name)
     d = device_inputs(wl, device)
+    norm = wl.with_norm
     touched = workload_bytes(wl, True)
     R = max(2, int(np.ceil(2 * L2_BYTES / touched)))
     R = min(R, 2048)
-    # R copies of every per-call operand at distinct addresses
-    xs = d["x"].unsqueeze(0).expand(R, *d["x"].shape).contiguous()
-    shs = d["shared"].unsqueeze(0).expand(R, *d["shared"].shape).contiguous()
-    outs = torch.empty((R, wl.T, wl.H), dtype=torch.bfloat16, device=device)
-    sets = [({"x": xs[r], "idx": d["idx"], "w": d["w"], "shared": shs[r]}, {"out": outs[r]})
-            for r in range(R)]
+
+    def rep(t):   # R copies at distinct addresses
+        return t.unsqueeze(0).expand(R, *t.shape).contiguous()
+
+    xs, shs = rep(d["x"]), rep(d["shared"])
+    rss = rep(d["residual"]) if norm else None
+    outs = {k: torch.empty((R, wl.T, wl.H), dtype=torch.bfloat16, device=device)
+            for k in (("out", "residual_out", "norm_out") if norm else ("out",))}
+    sets = []
+    for r in range(R):
+        dd = {"x": xs[r], "idx": d["idx"], "w": d["w"], "shared": shs[r]}
+        if norm:
+            dd["residual"], dd["gamma"] = rss[r], d["gamma"]
+        sets.append((dd, {k: v[r] for k, v in outs.items()}))
     bound = [mf.bind(dd["x"], dd["idx"], dd["w"], wl.wkind, dd["shared"],
-                     routed_scale=wl.routed_scale, out=oo["out"]) for dd, oo in sets]
+                     routed_scale=wl.routed_scale, residual=dd.get("residual"),
+                     gamma=dd.get("gamma"), eps=wl.eps, **oo) for dd, oo in sets]
+    ws = torch.empty(mf.unfused_workspace_bytes(wl.T, wl.H), dtype=torch.uint8, device=device)
 
     def one_pass():
         for dd, oo in sets:
@@ -246,8 +261,15 @@ def decode_latency(mf, name, device, reps):
         for f in bound:
             f()
 
+    def one_pass_unfused():
+        for dd, oo in sets:
+            mf.moe_finalize_unfused(dd["x"], dd["idx"], dd["w"], wl.wkind, dd["shared"],
+                                    routed_scale=wl.routed_scale, residual=dd.get("residual"),
+                                    gamma=dd.get("gamma"), eps=wl.eps, workspace=ws, **oo)
+
     one_pass()
     one_pass_bound()
+    one_pass_unfused()
     torch.cuda.synchronize(device)
     n_pass = max(1, reps // R)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -260,33 +282,38 @@ def decode_latency(mf, name, device, reps):
         torch.cuda.synchronize(device)
         return a.elapsed_time(b) * 1e3 / (n_pass * R)
 
+    def graph(fn):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device)
+        s.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                fn()
+        torch.cuda.current_stream(device).wait_stream(s)
+        g.replay()
+        torch.cuda.synchronize(device)
+        samples = []
+        for _ in range(5):
+            a.record()
+            for _ in range(n_pass):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize(device)
+            samples.append(a.elapsed_time(b) * 1e3 / (n_pass * R))
+        del g
+        return statistics.median(samples)
+
     eager_checked_us = eager(one_pass)      # argument checks on every call
     eager_us = eager(one_pass_bound)        # checked once, then raw C-ABI calls
-    # CUDA graph of one pass over all copies, replayed
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream(device)
-    s.wait_stream(torch.cuda.current_stream(device))
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            one_pass()
-    torch.cuda.current_stream(device).wait_stream(s)
-    g.replay()
-    torch.cuda.synchronize(device)
-    samples = []
-    for _ in range(5):
-        a.record()
-        for _ in range(n_pass):
-            g.replay()
-        b.record()
-        torch.cuda.synchronize(device)
-        samples.append(a.elapsed_time(b) * 1e3 / (n_pass * R))
-    graph_us = statistics.median(samples)
-    plan = mf.plan(wl.T, wl.K, wl.H, False, True,
+    graph_us = graph(one_pass)
+    unfused_us = graph(one_pass_unfused)
+    plan = mf.plan(wl.T, wl.K, wl.H, norm, True,
                    torch.cuda.get_device_properties(device).multi_processor_count)
-    del xs, shs, outs, g, bound
-    return {"T": wl.T, "K": wl.K, "H": wl.H, "routing": wl.wkind,
+    del xs, shs, rss, outs, bound, ws
+    return {"T": wl.T, "K": wl.K, "H": wl.H, "routing": wl.wkind, "rmsnorm": norm,
             "us_per_call_graph": round(graph_us, 3), "us_per_call_eager": round(eager_us, 3),
             "us_per_call_eager_checked": round(eager_checked_us, 3),
+            "unfused_us_per_call_graph": round(unfused_us, 3),
             "GBps_graph": round(touched / (graph_us * 1e-6) / 1e9, 1),
             "copies": R, "calls": n_pass * R, "plan": plan}
 
@@ -421,7 +448,8 @@ def run_ours(args, ws, rank, local):
     decode = {}
     if not args.skip_decode:
         decode = {"T1": decode_latency(mf, "decode_bs1_packed", device, 4000),
-                  "T256": decode_latency(mf, "decode_bs256", device, 2000)}
+                  "T256": decode_latency(mf, "decode_bs256", device, 2000),
+                  "T16_rmsnorm": decode_latency(mf, "fused_norm_bs16", device, 2000)}
 
     cpu = None
     if rank == 0 and not args.skip_cpu:

@@ -50,6 +50,7 @@
 #ifndef MOE_FINALIZE_H_
 #define MOE_FINALIZE_H_
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -185,6 +186,39 @@ moef_status moe_finalize_ex(const void *permuted_out, int64_t P,
                             int T, int K, int H,
                             int splits_hint, int threads_hint,
                             cudaStream_t stream);
+
+/*
+ * moe_finalize_unfused -- the same operation as moe_finalize, computed as
+ * separate kernels the way the pages' baselines ran it, for A/B measurement
+ * of the fusion ("Support deferred MoE finalize for MXFP4 and FP8
+ * block-scale", Speed: in-kernel combine + elementwise add for the shared
+ * expert; "[Kimi K2.5] Fuse deferred MoE finalize ...", Numerics & speed:
+ * finalize followed by a separate residual + RMSNorm kernel):
+ *
+ *   tmp = bf16(sum_k (w * routed_scale) * row)   (kernel 1, into workspace)
+ *   out = bf16(tmp + shared_out)                 (kernel 2)
+ *   residual_out = bf16(out + residual), norm_out from residual_out
+ *                                                (kernel 3, with a residual)
+ *
+ * Arguments and rules as for moe_finalize, except: out is always required
+ * (it is kernel 3's input), and `workspace` is a caller-owned device buffer
+ * of at least moe_finalize_unfused_workspace_bytes(T, H) bytes (else
+ * MOEF_ERR_NULL / MOEF_ERR_SHAPE), 2-byte aligned, not overlapping any
+ * other argument; its contents on entry do not matter and are overwritten.
+ * Results differ from moe_finalize by the intermediate bf16 roundings.
+ */
+size_t moe_finalize_unfused_workspace_bytes(int T, int H);
+
+moef_status moe_finalize_unfused(const void *permuted_out, int64_t P,
+                                 const int32_t *idx_map,
+                                 const void *weights, moef_weight_kind wkind,
+                                 float routed_scale,
+                                 const void *shared_out,
+                                 const void *residual, const void *gamma, float eps,
+                                 void *out, void *residual_out, void *norm_out,
+                                 int T, int K, int H,
+                                 void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
 
 /*
  * unpack_topk_ids -- split n packed routing words (expert_id << 16) |

@@ -58,6 +58,10 @@ def _lib():
         lib.moe_finalize.restype = i32
         lib.moe_finalize_ex.argtypes = common + [i32, i32, vp]
         lib.moe_finalize_ex.restype = i32
+        lib.moe_finalize_unfused.argtypes = common + [vp, ctypes.c_size_t, vp]
+        lib.moe_finalize_unfused.restype = i32
+        lib.moe_finalize_unfused_workspace_bytes.argtypes = [i32, i32]
+        lib.moe_finalize_unfused_workspace_bytes.restype = ctypes.c_size_t
         lib.moe_finalize_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
                                           ctypes.POINTER(Plan)]
         lib.moe_finalize_plan.restype = i32
@@ -175,6 +179,39 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
     st = _lib().moe_finalize_ex(*args, _stream(stream, permuted_out.device))
     if st != 0:
         raise MoefError(st, "moe_finalize")
+    return res
+
+
+def unfused_workspace_bytes(T: int, H: int) -> int:
+    """Bytes of workspace moe_finalize_unfused needs for T tokens of H values."""
+    return int(_lib().moe_finalize_unfused_workspace_bytes(int(T), int(H)))
+
+
+def moe_finalize_unfused(permuted_out: torch.Tensor, idx_map: torch.Tensor,
+                         weights: torch.Tensor, wkind: str, shared_out: torch.Tensor, *,
+                         routed_scale: float = 1.0, residual: Optional[torch.Tensor] = None,
+                         gamma: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                         out: Optional[torch.Tensor] = None,
+                         residual_out: Optional[torch.Tensor] = None,
+                         norm_out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """The finalize as separate kernels (combine, shared add, residual +
+    RMSNorm) with a bf16 intermediate in ``workspace`` (allocated when not
+    given): the A/B baseline of the fused ``moe_finalize``.  Same arguments;
+    ``out`` is always produced."""
+    args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
+                         residual, gamma, eps, out, residual_out, norm_out, True, 0, 0)
+    T, H = idx_map.shape[0], permuted_out.shape[1]
+    need = unfused_workspace_bytes(T, H)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=permuted_out.device)
+    if workspace.device != permuted_out.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the same device")
+    nbytes = workspace.numel() * workspace.element_size()
+    st = _lib().moe_finalize_unfused(*args[:16], _ptr(workspace), nbytes,
+                                     _stream(stream, permuted_out.device))
+    if st != 0:
+        raise MoefError(st, "moe_finalize_unfused")
     return res
 
 

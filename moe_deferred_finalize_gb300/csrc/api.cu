@@ -144,16 +144,18 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, in
     return MOEF_OK;
 }
 
-moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *idx_map,
-                            const void *weights, moef_weight_kind wkind, float routed_scale,
-                            const void *shared_out, const void *residual, const void *gamma,
-                            float eps, void *out, void *residual_out, void *norm_out,
-                            int T, int K, int H, int splits_hint, int threads_hint,
-                            cudaStream_t stream) {
+namespace {
+
+// Checks shared by every finalize entry point; fills `p` (all but the plan
+// fields) and reports whether the 16-byte path applies.
+moef_status check_finalize_args(const void *permuted_out, int64_t P, const int32_t *idx_map,
+                                const void *weights, moef_weight_kind wkind, float routed_scale,
+                                const void *shared_out, const void *residual, const void *gamma,
+                                float eps, void *out, void *residual_out, void *norm_out,
+                                int T, int K, int H, moef::FinalizeParams *p, bool *vec_ok) {
     if (T < 0 || K < 1 || K > MOEF_MAX_K || H < 1) return MOEF_ERR_SHAPE;
     if (wkind != MOEF_W_FP32 && wkind != MOEF_W_BF16 && wkind != MOEF_W_PACKED_TOPK)
         return MOEF_ERR_ARG;
-    if (splits_hint < 0 || threads_hint < 0) return MOEF_ERR_ARG;
     if (T == 0) return MOEF_OK;
     if (P < 1) return MOEF_ERR_SHAPE;
     if (!permuted_out || !idx_map || !weights || !shared_out) return MOEF_ERR_NULL;
@@ -175,37 +177,94 @@ moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *
     if (!aligned(idx_map, 4)) return MOEF_ERR_ALIGN;
     if (!aligned(weights, wkind == MOEF_W_BF16 ? 2 : 4)) return MOEF_ERR_ALIGN;
 
-    bool vec_ok = (H % 8) == 0;
+    bool v = (H % 8) == 0;
     for (const void *q : bf16_ptrs)
-        if (q && !aligned(q, 16)) vec_ok = false;
+        if (q && !aligned(q, 16)) v = false;
+    *vec_ok = v;
+
+    p->x = static_cast<const uint16_t *>(permuted_out);
+    p->idx = idx_map;
+    p->weights = weights;
+    p->shared = static_cast<const uint16_t *>(shared_out);
+    p->residual = static_cast<const uint16_t *>(residual);
+    p->gamma = static_cast<const uint16_t *>(gamma);
+    p->out = static_cast<uint16_t *>(out);
+    p->residual_out = static_cast<uint16_t *>(residual_out);
+    p->norm_out = static_cast<uint16_t *>(norm_out);
+    p->routed_scale = routed_scale;
+    p->eps = eps;
+    p->wkind = static_cast<int>(wkind);
+    p->T = T;
+    p->K = K;
+    p->H = H;
+    return MOEF_OK;
+}
+
+void apply_plan(const moef_plan &plan, moef::FinalizeParams *p) {
+    p->nvec = p->H / plan.vec;
+    p->splits = plan.splits;
+    p->slice = plan.slice;
+}
+
+}  // namespace
+
+moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *idx_map,
+                            const void *weights, moef_weight_kind wkind, float routed_scale,
+                            const void *shared_out, const void *residual, const void *gamma,
+                            float eps, void *out, void *residual_out, void *norm_out,
+                            int T, int K, int H, int splits_hint, int threads_hint,
+                            cudaStream_t stream) {
+    if (splits_hint < 0 || threads_hint < 0) return MOEF_ERR_ARG;
+    moef::FinalizeParams p;
+    bool vec_ok = false;
+    moef_status st = check_finalize_args(permuted_out, P, idx_map, weights, wkind, routed_scale,
+                                         shared_out, residual, gamma, eps, out, residual_out,
+                                         norm_out, T, K, H, &p, &vec_ok);
+    if (st != MOEF_OK || T == 0) return st;
 
     int sms = 0;
     if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
     moef_plan plan;
-    const moef_status st = moe_finalize_plan(T, K, H, norm ? 1 : 0, vec_ok ? 1 : 0, sms,
-                                             splits_hint, threads_hint, &plan);
+    st = moe_finalize_plan(T, K, H, residual ? 1 : 0, vec_ok ? 1 : 0, sms, splits_hint,
+                           threads_hint, &plan);
     if (st != MOEF_OK) return st;
-
-    moef::FinalizeParams p;
-    p.x = static_cast<const uint16_t *>(permuted_out);
-    p.idx = idx_map;
-    p.weights = weights;
-    p.shared = static_cast<const uint16_t *>(shared_out);
-    p.residual = static_cast<const uint16_t *>(residual);
-    p.gamma = static_cast<const uint16_t *>(gamma);
-    p.out = static_cast<uint16_t *>(out);
-    p.residual_out = static_cast<uint16_t *>(residual_out);
-    p.norm_out = static_cast<uint16_t *>(norm_out);
-    p.routed_scale = routed_scale;
-    p.eps = eps;
-    p.wkind = static_cast<int>(wkind);
-    p.T = T;
-    p.K = K;
-    p.H = H;
-    p.nvec = H / plan.vec;
-    p.splits = plan.splits;
-    p.slice = plan.slice;
+    apply_plan(plan, &p);
     return moef::launch_finalize(p, plan, stream) == cudaSuccess ? MOEF_OK : MOEF_ERR_CUDA;
+}
+
+size_t moe_finalize_unfused_workspace_bytes(int T, int H) {
+    if (T <= 0 || H <= 0) return 0;
+    return static_cast<size_t>(T) * static_cast<size_t>(H) * 2u;
+}
+
+moef_status moe_finalize_unfused(const void *permuted_out, int64_t P, const int32_t *idx_map,
+                                 const void *weights, moef_weight_kind wkind,
+                                 float routed_scale, const void *shared_out,
+                                 const void *residual, const void *gamma, float eps, void *out,
+                                 void *residual_out, void *norm_out, int T, int K, int H,
+                                 void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    moef::FinalizeParams p;
+    bool vec_ok = false;
+    moef_status st = check_finalize_args(permuted_out, P, idx_map, weights, wkind, routed_scale,
+                                         shared_out, residual, gamma, eps, out, residual_out,
+                                         norm_out, T, K, H, &p, &vec_ok);
+    if (st != MOEF_OK || T == 0) return st;
+    if (!out) return MOEF_ERR_NULL;              // the unfused path always writes out
+    if (!workspace) return MOEF_ERR_NULL;
+    if (workspace_bytes < moe_finalize_unfused_workspace_bytes(T, H)) return MOEF_ERR_SHAPE;
+    if (!aligned(workspace, 2)) return MOEF_ERR_ALIGN;
+    if (!aligned(workspace, 16)) vec_ok = false;
+
+    int sms = 0;
+    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
+    moef_plan plan;
+    st = moe_finalize_plan(T, K, H, 0, vec_ok ? 1 : 0, sms, 0, 0, &plan);
+    if (st != MOEF_OK) return st;
+    apply_plan(plan, &p);
+    return moef::launch_unfused(p, plan, static_cast<uint16_t *>(workspace), sms, stream) ==
+                   cudaSuccess
+               ? MOEF_OK
+               : MOEF_ERR_CUDA;
 }
 
 moef_status moe_finalize(const void *permuted_out, int64_t P, const int32_t *idx_map,

@@ -34,6 +34,11 @@ struct FinalizeParams {
 cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan,
                             cudaStream_t stream);
 
+// Launches the unfused three-kernel finalize (combine into tmp, add the
+// shared output, residual + RMSNorm); `plan` is a plan without RMSNorm.
+cudaError_t launch_unfused(const FinalizeParams &p, const moef_plan &plan, uint16_t *tmp,
+                           int num_sms, cudaStream_t stream);
+
 cudaError_t launch_unpack(const int32_t *packed, int64_t n, int32_t *expert_ids,
                           float *weights, int num_sms, cudaStream_t stream);
 
