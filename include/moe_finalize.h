@@ -221,6 +221,44 @@ moef_status moe_finalize_unfused(const void *permuted_out, int64_t P,
                                  cudaStream_t stream);
 
 /*
+ * moe_finalize_unfused_noalloc -- moe_finalize_unfused without a workspace
+ * argument, for callers that cannot allocate device memory: code running
+ * while a CUDA graph is being captured (cudaMalloc is not allowed there),
+ * serving engines that fix every device allocation before they start and
+ * forbid allocation on the request path, and plugins whose host framework
+ * owns all device memory and gives them no allocator.  The pages have no
+ * counterpart to this entry point.
+ *
+ * The workspace is a fixed array of MOEF_NOALLOC_SCRATCH_BYTES (8 MiB)
+ * compiled into the library; every GPU on which the library's device code
+ * is loaded holds it until the process exits.  Requests needing more,
+ * T * H * 2 > MOEF_NOALLOC_SCRATCH_BYTES (T > 585 at H = 7168), return
+ * MOEF_ERR_SHAPE without enqueuing anything.  The call allocates nothing
+ * (no cudaMalloc, no library allocator).
+ *
+ * Set-up: the first call made on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.
+ *
+ * Sharing: all calls on a device use the same array, and it keeps whatever
+ * the last call left in it.  Nothing in it needs to start at zero (the first
+ * kernel writes every byte the second reads), but two calls whose kernels
+ * overlap on the GPU (e.g. on two streams without ordering) race on it:
+ * order them.  Arguments, rules and results are otherwise those of
+ * moe_finalize_unfused.
+ */
+#define MOEF_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+moef_status moe_finalize_unfused_noalloc(const void *permuted_out, int64_t P,
+                                         const int32_t *idx_map,
+                                         const void *weights, moef_weight_kind wkind,
+                                         float routed_scale,
+                                         const void *shared_out,
+                                         const void *residual, const void *gamma, float eps,
+                                         void *out, void *residual_out, void *norm_out,
+                                         int T, int K, int H, cudaStream_t stream);
+
+/*
  * unpack_topk_ids -- split n packed routing words (expert_id << 16) |
  * bf16(weight) ("[Deepseek V4] Keep fp32 routing weights in the mxfp4
  * trtllm MoE", description) into expert ids (the high 16 bits as an

@@ -60,6 +60,8 @@ def _lib():
         lib.moe_finalize_ex.restype = i32
         lib.moe_finalize_unfused.argtypes = common + [vp, ctypes.c_size_t, vp]
         lib.moe_finalize_unfused.restype = i32
+        lib.moe_finalize_unfused_noalloc.argtypes = common + [vp]
+        lib.moe_finalize_unfused_noalloc.restype = i32
         lib.moe_finalize_unfused_workspace_bytes.argtypes = [i32, i32]
         lib.moe_finalize_unfused_workspace_bytes.restype = ctypes.c_size_t
         lib.moe_finalize_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
@@ -212,6 +214,36 @@ def moe_finalize_unfused(permuted_out: torch.Tensor, idx_map: torch.Tensor,
                                      _stream(stream, permuted_out.device))
     if st != 0:
         raise MoefError(st, "moe_finalize_unfused")
+    return res
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def moe_finalize_unfused_noalloc(permuted_out: torch.Tensor, idx_map: torch.Tensor,
+                                 weights: torch.Tensor, wkind: str, shared_out: torch.Tensor,
+                                 *, routed_scale: float = 1.0,
+                                 residual: Optional[torch.Tensor] = None,
+                                 gamma: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                                 out: torch.Tensor, residual_out: Optional[torch.Tensor] = None,
+                                 norm_out: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """``moe_finalize_unfused`` for callers that cannot allocate device
+    memory (inside graph capture, fixed-memory serving engines, plugins with
+    no allocator): the workspace is the library's fixed 8 MiB scratch array,
+    so T * H * 2 must not exceed ``NOALLOC_SCRATCH_BYTES``.  All outputs must
+    be given (this wrapper allocates nothing either).  Calls on one device
+    share the scratch: order them (one stream, or events)."""
+    T, H = idx_map.shape[0], permuted_out.shape[1]
+    if T * H * 2 > NOALLOC_SCRATCH_BYTES:
+        raise ValueError(f"T*H*2 = {T * H * 2} bytes exceed the fixed scratch of "
+                         f"{NOALLOC_SCRATCH_BYTES} bytes")
+    if residual is not None and (residual_out is None or norm_out is None):
+        raise ValueError("with a residual, residual_out and norm_out must be given")
+    args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
+                         residual, gamma, eps, out, residual_out, norm_out, True, 0, 0)
+    st = _lib().moe_finalize_unfused_noalloc(*args[:16], _stream(stream, permuted_out.device))
+    if st != 0:
+        raise MoefError(st, "moe_finalize_unfused_noalloc")
     return res
 
 
