@@ -44,6 +44,10 @@ class Oracle:
         lib.oref_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.oref_rmsnorm_bf16.restype = None
         lib.oref_rmsnorm_bf16.argtypes = [p, p, ctypes.c_double, i64, i64, p]
+        lib.oref_pack_topk_ids.restype = None
+        lib.oref_pack_topk_ids.argtypes = [p, p, i64, p]
+        lib.oref_topk_route.restype = ctypes.c_int
+        lib.oref_topk_route.argtypes = [p, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p]
         self.lib = lib
 
     def moe_finalize(self, permuted_out, idx, weights, wkind, routed_scale, shared,
@@ -111,6 +115,28 @@ class Oracle:
         """One packed word (expert_id << 16) | bf16_rne(weight), as int32."""
         return int(self.lib.oref_pack_topk_id(int(expert_id), float(weight)))
 
+    def pack_topk_ids(self, expert_ids, weights):
+        """Packed words for arrays of expert ids (int32) and fp32 weights."""
+        e = _c(expert_ids, np.int32)
+        w = _c(weights, np.float32)
+        out = np.empty(e.shape, np.int32)
+        self.lib.oref_pack_topk_ids(_ptr(e), _ptr(w), e.size, _ptr(out))
+        return out
+
+    def topk_route(self, logits, K, kind):
+        """Top-K gate over fp32 logits [T, E]: (ids int32 [T, K] in
+        descending logit order, ties lowest id first; weights float64 [T, K],
+        kind "softmax" or "sigmoid" over the selected logits)."""
+        z = _c(logits, np.float32)
+        T, E = z.shape
+        ids = np.empty((T, K), np.int32)
+        w = np.empty((T, K), np.float64)
+        rc = self.lib.oref_topk_route(_ptr(z), T, E, K, {"softmax": 0, "sigmoid": 1}[kind],
+                                      _ptr(ids), _ptr(w))
+        if rc != 0:
+            raise ValueError("bad sizes or kind")
+        return ids, w
+
     def f32_to_bf16(self, x):
         """fp32 -> bf16 bits, round to nearest even, one value at a time."""
         flat = np.asarray(x, np.float32).ravel()
@@ -148,3 +174,11 @@ def pack_topk_id(expert_id, weight):
 
 def f32_to_bf16(x):
     return default().f32_to_bf16(x)
+
+
+def pack_topk_ids(expert_ids, weights):
+    return default().pack_topk_ids(expert_ids, weights)
+
+
+def topk_route(logits, K, kind):
+    return default().topk_route(logits, K, kind)

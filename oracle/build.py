@@ -11,6 +11,7 @@ import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "finalize_ref.c")
+SOURCES = [SRC, os.path.join(HERE, "routing_ref.c")]
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liboracle.so")
 
@@ -19,10 +20,11 @@ _FLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
           "-shared", "-fPIC", "-Wall", "-Wextra"]
 
 
-def compile_source(src_path: str, lib_path: str) -> str:
-    """Compile one C source with the oracle's flags into ``lib_path``."""
+def compile_source(src_path, lib_path: str) -> str:
+    """Compile C source(s) with the oracle's flags into ``lib_path``."""
+    srcs = [src_path] if isinstance(src_path, str) else list(src_path)
     tmp = lib_path + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", *_FLAGS, "-o", tmp, src_path, "-lm"], check=True)
+    subprocess.run(["gcc", *_FLAGS, "-o", tmp, *srcs, "-lm"], check=True)
     os.replace(tmp, lib_path)
     return lib_path
 
@@ -30,10 +32,10 @@ def compile_source(src_path: str, lib_path: str) -> str:
 def build_oracle(force: bool = False) -> str:
     """Build ``_build/liboracle.so`` if it is missing or older than its source."""
     if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
+            and all(os.path.getmtime(LIB) >= os.path.getmtime(s) for s in SOURCES)):
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
-    return compile_source(SRC, LIB)
+    return compile_source(SOURCES, LIB)
 
 
 if __name__ == "__main__":

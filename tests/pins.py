@@ -280,4 +280,71 @@ def pin_bf16_rounding_library(orc):
     assert np.isnan(bf16_bits_to_f32(qnan)).all() and ((qnan & 0x0040) != 0).all()
 
 
+
+
+# ------------------------------------------------------------ routing pins
+
+
+def pin_route_golden(orc):
+    g = _load("routing_gate_hand.json")
+    z = np.array([g["logits"]], np.float32)
+    ids, w = orc.topk_route(z, 3, "softmax")
+    assert ids[0].tolist() == g["ids_k3"], ids
+    e3 = math.exp(-3.0)
+    want = np.array([1.0, e3, e3]) / (1.0 + 2.0 * e3)
+    assert np.allclose(w[0], want, rtol=1e-15, atol=0), w
+    ids, w = orc.topk_route(z, 3, "sigmoid")
+    s = lambda v: 1.0 / (1.0 + math.exp(-v))
+    want = np.array([s(5), s(2), s(2)]) / (s(5) + 2 * s(2))
+    assert ids[0].tolist() == g["ids_k3"] and np.allclose(w[0], want, rtol=1e-15, atol=0)
+    ids, _ = orc.topk_route(z, 5, "softmax")
+    assert ids[0].tolist() == g["ids_k5"], ids
+
+
+def pin_route_equal_logits(orc):
+    """All logits equal: experts 0..K-1, every weight 1/K, for both rules."""
+    z = np.full((3, 16), 0.75, np.float32)
+    for kind in ("softmax", "sigmoid"):
+        ids, w = orc.topk_route(z, 5, kind)
+        assert (ids == np.arange(5)).all()
+        assert np.allclose(w, 0.2, rtol=1e-15, atol=0)
+
+
+def pin_route_library_order(orc):
+    """Selection equals numpy's stable descending sort, also with many ties."""
+    rng = np.random.default_rng(14)
+    for z in (rng.standard_normal((40, 256)).astype(np.float32),
+              (np.round(rng.standard_normal((40, 256)) * 2) / 2).astype(np.float32)):
+        ids, _ = orc.topk_route(z, 8, "sigmoid")
+        ref = np.argsort(-z, axis=1, kind="stable")[:, :8]
+        assert np.array_equal(ids, ref)
+
+
+def pin_route_library_weights(orc):
+    """Weights equal scipy's softmax / expit over the selected logits."""
+    from scipy.special import expit, softmax
+    rng = np.random.default_rng(15)
+    z = (3 * rng.standard_normal((30, 384))).astype(np.float32)
+    ids, w = orc.topk_route(z, 8, "softmax")
+    sel = np.take_along_axis(z, ids, axis=1).astype(np.float64)
+    assert np.allclose(w, softmax(sel, axis=1), rtol=1e-13, atol=0)
+    ids, w = orc.topk_route(z, 8, "sigmoid")
+    sel = np.take_along_axis(z, ids, axis=1).astype(np.float64)
+    e = expit(sel)
+    assert np.allclose(w, e / e.sum(axis=1, keepdims=True), rtol=1e-13, atol=0)
+
+
+def pin_pack_array_library(orc):
+    """Array packing: high half the expert id, low half torch's bf16 of the weight."""
+    rng = np.random.default_rng(16)
+    ids = rng.integers(0, 65536, 5000).astype(np.int32)
+    ties = ((rng.integers(0, 2**16, 1000) << 16) | 0x8000).astype(np.uint32).view(np.float32)
+    w = np.concatenate([rng.random(4000).astype(np.float32), ties])
+    w[~np.isfinite(w)] = np.float32(0.5)
+    got = orc.pack_topk_ids(ids, w).view(np.uint32)
+    ref_lo = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got >> 16, ids.astype(np.uint32))
+    assert np.array_equal((got & 0xFFFF).astype(np.uint16), ref_lo)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -6,7 +6,7 @@ import os
 import pytest
 
 import oracle
-from oracle.build import SRC, compile_source
+from oracle.build import SOURCES, compile_source
 
 import pins
 
@@ -53,15 +53,31 @@ MUTANTS = [
 ]
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_mutant(tmp_path, name, old, new):
-    src = open(SRC).read()
+ROUTING_MUTANTS = [
+    ("route_ties_keep_higher_id", "if (best < 0 || z[e] > z[best])",
+     "if (best < 0 || z[e] >= z[best])"),
+    ("route_selects_smallest", "if (best < 0 || z[e] > z[best])",
+     "if (best < 0 || z[e] < z[best])"),
+    ("route_sigmoid_sign", "w[k] = 1.0 / (1.0 + exp(-(double)z[ids[k]]));",
+     "w[k] = 1.0 / (1.0 + exp((double)z[ids[k]]));"),
+    ("route_not_normalised", "for (int k = 0; k < K; ++k) w[k] /= total;", ""),
+    ("pack_array_swaps_operands", "packed[i] = oref_pack_topk_id(expert_ids[i], weights[i]);",
+     "packed[i] = oref_pack_topk_id((int32_t)weights[i], (float)expert_ids[i]);"),
+]
+ALL = [(n, o, r, 0) for n, o, r in MUTANTS] + [(n, o, r, 1) for n, o, r in ROUTING_MUTANTS]
+
+
+@pytest.mark.parametrize("name,old,new,which", ALL, ids=[m[0] for m in ALL])
+def test_pins_catch_mutant(tmp_path, name, old, new, which):
+    src = open(SOURCES[which]).read()
     assert src.count(old) >= 1, f"mutation site for {name} not found"
     mutated = src.replace(old, new)
     path = os.path.join(tmp_path, f"{name}.c")
     with open(path, "w") as f:
         f.write(mutated)
-    lib = compile_source(path, os.path.join(tmp_path, f"lib{name}.so"))
+    srcs = list(SOURCES)
+    srcs[which] = path
+    lib = compile_source(srcs, os.path.join(tmp_path, f"lib{name}.so"))
     orc = oracle.Oracle(lib)
     caught = []
     for pin in pins.ALL_PINS:
