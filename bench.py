@@ -318,6 +318,54 @@ def decode_latency(mf, name, device, reps):
             "copies": R, "calls": n_pass * R, "plan": plan}
 
 
+def gate_latency(mf, device, T, E=256, K=8, calls=2000):
+    """µs per top-K gate call (logits -> ids, fp32 weights, packed words),
+    CUDA-graph replay over rotating logits copies larger than L2 when they fit."""
+    per = T * E * 4
+    R = int(min(max(2, np.ceil(2 * L2_BYTES / per)), 4096))
+    g_ = torch.Generator(device=device).manual_seed(T)
+    z = torch.randn((R, T, E), generator=g_, device=device, dtype=torch.float32)
+    outs = [(torch.empty((T, K), dtype=torch.int32, device=device),
+             torch.empty((T, K), dtype=torch.float32, device=device),
+             torch.empty((T, K), dtype=torch.int32, device=device)) for _ in range(R)]
+    lib = mf.lib()
+    import ctypes
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    args = [(P(z[r]), P(outs[r][0]), P(outs[r][1]), P(outs[r][2])) for r in range(R)]
+
+    def one_pass(stream):
+        sv = ctypes.c_void_p(stream.cuda_stream)
+        for a_ in args:
+            st = lib.moe_topk_route(a_[0], T, E, K, 1, a_[1], a_[2], a_[3], sv)
+            if st != 0:
+                raise RuntimeError(f"moe_topk_route status {st}")
+
+    cur = torch.cuda.current_stream(device)
+    one_pass(cur)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(cur)
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            one_pass(s)
+    cur.wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize(device)
+    n_pass = max(1, calls // R)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    samples = []
+    for _ in range(3):
+        a.record()
+        for _ in range(n_pass):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize(device)
+        samples.append(a.elapsed_time(b) * 1e3 / (n_pass * R))
+    del g, z, outs
+    return round(statistics.median(samples), 3)
+
+
 def e2e(mf, wl, host, device, steps):
     """GB/s with host inputs: per step, H2D of every input, the call, D2H of
     the results, all inside the timed region."""
@@ -451,6 +499,12 @@ def run_ours(args, ws, rank, local):
                   "T256": decode_latency(mf, "decode_bs256", device, 2000),
                   "T16_rmsnorm": decode_latency(mf, "fused_norm_bs16", device, 2000)}
 
+    gate = {}
+    if not args.skip_decode:
+        gate = {"E": 256, "K": 8, "kind": "sigmoid", "outputs": "ids, fp32 weights, packed",
+                "us_per_call_graph": {f"T{T}": gate_latency(mf, device, T)
+                                      for T in (1, 256, 16384)}}
+
     cpu = None
     if rank == 0 and not args.skip_cpu:
         gbps, sec, passes = oracle_gbps(wl, np.arange(wl.T), repeat_until_s=10.0)
@@ -481,6 +535,7 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
         "gpu_launches": args.steps,
         "decode": decode,
+        "gate": gate,
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -259,6 +259,44 @@ moef_status moe_finalize_unfused_noalloc(const void *permuted_out, int64_t P,
                                          int T, int K, int H, cudaStream_t stream);
 
 /*
+ * Routing gate: the producer of the routing weights the finalize consumes
+ * ("[Deepseek V4] Keep fp32 routing weights in the mxfp4 trtllm MoE",
+ * description: a fused gate kernel yields fp32 routing weights, and a
+ * separate packing launch turns them into (expert_id << 16) | bf16(weight)
+ * words).  The pages do not define the gate; this one takes, per token,
+ * the K largest of E logits in descending order (equal logits: lowest
+ * expert id first) and weights them over the K selected logits z_k by
+ *   MOEF_GATE_SOFTMAX: w_k = exp(z_k - max z) / sum_j exp(z_j - max z)
+ *   MOEF_GATE_SIGMOID: w_k = s(z_k) / sum_j s(z_j),  s(z) = 1 / (1 + exp(-z))
+ * in fp32.  The expert ids are exact; the weights carry fp32 rounding.
+ */
+typedef enum { MOEF_GATE_SOFTMAX = 0, MOEF_GATE_SIGMOID = 1 } moef_gate_kind;
+
+/* Largest expert count the gate accepts. */
+#define MOEF_MAX_EXPERTS 1024
+
+/*
+ * moe_topk_route -- the gate above.  logits: fp32 [T, E], finite.
+ * Outputs, each [T, K] and each nullable (at least one non-NULL):
+ * expert_ids int32; weights fp32; packed int32 (expert_id << 16) |
+ * bf16(weight), the bf16 rounded to nearest even from the fp32 weight
+ * written to `weights`.  1 <= K <= min(E, MOEF_MAX_K), 1 <= E <=
+ * MOEF_MAX_EXPERTS, T >= 0 (T = 0 enqueues nothing).  One warp per token.
+ */
+moef_status moe_topk_route(const float *logits, int T, int E, int K, moef_gate_kind kind,
+                           int32_t *expert_ids, float *weights, int32_t *packed,
+                           cudaStream_t stream);
+
+/*
+ * pack_topk_ids -- n words (expert_id << 16) | bf16(weight) from expert ids
+ * (int32, used modulo 65536) and fp32 weights; bf16 rounds to nearest even,
+ * a NaN keeps its upper payload bits with the quiet bit set.  Bit-exact.
+ * The three arrays must not overlap.  n = 0 enqueues nothing.
+ */
+moef_status pack_topk_ids(const int32_t *expert_ids, const float *weights, int64_t n,
+                          int32_t *packed, cudaStream_t stream);
+
+/*
  * unpack_topk_ids -- split n packed routing words (expert_id << 16) |
  * bf16(weight) ("[Deepseek V4] Keep fp32 routing weights in the mxfp4
  * trtllm MoE", description) into expert ids (the high 16 bits as an

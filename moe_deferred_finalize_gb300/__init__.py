@@ -8,10 +8,10 @@ kernels and their C ABI live in ``libmoe_finalize.so``
 (``include/moe_finalize.h``); this package is its thin Python binding.
 """
 from ._abi import (WKIND, BoundFinalize, MoefError, bind, check_indices, lib,  # noqa: F401
-                   moe_finalize, moe_finalize_unfused, moe_finalize_unfused_noalloc, plan,
-                   unfused_workspace_bytes, unpack_topk_ids)
+                   moe_finalize, moe_finalize_unfused, moe_finalize_unfused_noalloc,
+                   pack_topk_ids, plan, topk_route, unfused_workspace_bytes, unpack_topk_ids)
 
 __all__ = ["moe_finalize", "bind", "BoundFinalize", "moe_finalize_unfused",
-           "moe_finalize_unfused_noalloc",
+           "moe_finalize_unfused_noalloc", "topk_route", "pack_topk_ids",
            "unfused_workspace_bytes", "unpack_topk_ids", "check_indices", "plan", "lib",
            "MoefError", "WKIND"]

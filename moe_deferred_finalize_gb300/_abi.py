@@ -67,6 +67,10 @@ def _lib():
         lib.moe_finalize_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
                                           ctypes.POINTER(Plan)]
         lib.moe_finalize_plan.restype = i32
+        lib.moe_topk_route.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
+        lib.moe_topk_route.restype = i32
+        lib.pack_topk_ids.argtypes = [vp, vp, i64, vp, vp]
+        lib.pack_topk_ids.restype = i32
         lib.unpack_topk_ids.argtypes = [vp, i64, vp, vp, vp]
         lib.unpack_topk_ids.restype = i32
         lib.moe_finalize_check_indices.argtypes = [vp, i32, i32, i64, vp, vp]
@@ -294,6 +298,53 @@ def plan(T: int, K: int, H: int, with_norm: bool, vec_ok: bool = True, num_sms: 
     if st != 0:
         raise MoefError(st, "moe_finalize_plan")
     return p.as_dict()
+
+
+GATE = {"softmax": 0, "sigmoid": 1}
+
+
+def topk_route(logits: torch.Tensor, K: int, kind: str = "sigmoid", *,
+               want_ids: bool = True, want_weights: bool = True, want_packed: bool = False,
+               stream=None) -> dict:
+    """Top-K gate over fp32 logits [T, E] (see include/moe_finalize.h):
+    returns the requested of "expert_ids" int32 [T, K], "weights" fp32
+    [T, K] and "packed" int32 [T, K] words."""
+    if kind not in GATE:
+        raise ValueError(f"kind must be one of {sorted(GATE)}")
+    if logits.device.type != "cuda" or logits.dtype != torch.float32 or logits.dim() != 2 \
+            or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous float32 [T, E] CUDA tensor")
+    T, E = logits.shape
+    dev = logits.device
+    res = {}
+    if want_ids:
+        res["expert_ids"] = torch.empty((T, K), dtype=torch.int32, device=dev)
+    if want_weights:
+        res["weights"] = torch.empty((T, K), dtype=torch.float32, device=dev)
+    if want_packed:
+        res["packed"] = torch.empty((T, K), dtype=torch.int32, device=dev)
+    st = _lib().moe_topk_route(_ptr(logits), T, E, int(K), GATE[kind], _ptr(res.get("expert_ids")),
+                               _ptr(res.get("weights")), _ptr(res.get("packed")),
+                               _stream(stream, dev))
+    if st != 0:
+        raise MoefError(st, "moe_topk_route")
+    return res
+
+
+def pack_topk_ids(expert_ids: torch.Tensor, weights: torch.Tensor,
+                  packed: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """(expert_id << 16) | bf16_rne(weight) words, same shape as the inputs."""
+    dev = expert_ids.device
+    _check(expert_ids, "expert_ids", (torch.int32,), expert_ids.shape, dev)
+    _check(weights, "weights", (torch.float32,), expert_ids.shape, dev)
+    if packed is None:
+        packed = torch.empty_like(expert_ids)
+    _check(packed, "packed", (torch.int32,), expert_ids.shape, dev)
+    st = _lib().pack_topk_ids(_ptr(expert_ids), _ptr(weights), expert_ids.numel(), _ptr(packed),
+                              _stream(stream, dev))
+    if st != 0:
+        raise MoefError(st, "pack_topk_ids")
+    return packed
 
 
 def unpack_topk_ids(packed: torch.Tensor, expert_ids: Optional[torch.Tensor] = None,

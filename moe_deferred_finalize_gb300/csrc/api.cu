@@ -277,6 +277,37 @@ moef_status moe_finalize(const void *permuted_out, int64_t P, const int32_t *idx
                            stream);
 }
 
+moef_status moe_topk_route(const float *logits, int T, int E, int K, moef_gate_kind kind,
+                           int32_t *expert_ids, float *weights, int32_t *packed,
+                           cudaStream_t stream) {
+    if (T < 0 || E < 1 || E > MOEF_MAX_EXPERTS || K < 1 || K > MOEF_MAX_K || K > E)
+        return MOEF_ERR_SHAPE;
+    if (kind != MOEF_GATE_SOFTMAX && kind != MOEF_GATE_SIGMOID) return MOEF_ERR_ARG;
+    if (T == 0) return MOEF_OK;
+    if (!logits || (!expert_ids && !weights && !packed)) return MOEF_ERR_NULL;
+    if (!aligned(logits, 4) || (expert_ids && !aligned(expert_ids, 4)) ||
+        (weights && !aligned(weights, 4)) || (packed && !aligned(packed, 4)))
+        return MOEF_ERR_ALIGN;
+    return moef::launch_topk_route(logits, T, E, K, static_cast<int>(kind), expert_ids, weights,
+                                   packed, stream) == cudaSuccess
+               ? MOEF_OK
+               : MOEF_ERR_CUDA;
+}
+
+moef_status pack_topk_ids(const int32_t *expert_ids, const float *weights, int64_t n,
+                          int32_t *packed, cudaStream_t stream) {
+    if (n < 0) return MOEF_ERR_SHAPE;
+    if (n == 0) return MOEF_OK;
+    if (!expert_ids || !weights || !packed) return MOEF_ERR_NULL;
+    if (!aligned(expert_ids, 4) || !aligned(weights, 4) || !aligned(packed, 4))
+        return MOEF_ERR_ALIGN;
+    int sms = 0;
+    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
+    return moef::launch_pack(expert_ids, weights, n, packed, sms, stream) == cudaSuccess
+               ? MOEF_OK
+               : MOEF_ERR_CUDA;
+}
+
 moef_status unpack_topk_ids(const int32_t *packed, int64_t n, int32_t *expert_ids,
                             float *weights_f32, cudaStream_t stream) {
     if (n < 0) return MOEF_ERR_SHAPE;

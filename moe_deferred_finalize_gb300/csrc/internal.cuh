@@ -39,6 +39,13 @@ cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan,
 cudaError_t launch_unfused(const FinalizeParams &p, const moef_plan &plan, uint16_t *tmp,
                            int num_sms, cudaStream_t stream);
 
+cudaError_t launch_pack(const int32_t *expert_ids, const float *weights, int64_t n,
+                        int32_t *packed, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_topk_route(const float *logits, int T, int E, int K, int kind,
+                              int32_t *expert_ids, float *weights, int32_t *packed,
+                              cudaStream_t stream);
+
 cudaError_t launch_unpack(const int32_t *packed, int64_t n, int32_t *expert_ids,
                           float *weights, int num_sms, cudaStream_t stream);
 

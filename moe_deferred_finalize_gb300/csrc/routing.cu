@@ -1,14 +1,20 @@
-// Routing-word kernels: unpacking (expert_id << 16) | bf16(weight) words and
-// counting out-of-range entries of the [token, top_k] row map.
+// Routing kernels: the top-K gate that produces routing weights, packing and
+// unpacking of (expert_id << 16) | bf16(weight) words, and counting
+// out-of-range entries of the [token, top_k] row map.
 //
 // Packed format: "[Deepseek V4] Keep fp32 routing weights in the mxfp4
 // trtllm MoE", description.  Row-map bounds: "[Kimi K2.5] Fuse deferred MoE
 // finalize into next-layer AR + residual + RMSNorm", Key modifications (a
 // flat index map read with the wrong top_k went out of bounds).
 //
-// Both are small elementwise passes over T*K words (grid-stride loops,
-// grids capped at a few CTAs per SM); they are bound by launch latency,
-// not by bandwidth.
+// Pack, unpack and check are small elementwise passes over T*K words
+// (grid-stride loops, grids capped at a few CTAs per SM); the gate reads
+// T*E logits once, one warp per token.  All are bound by launch latency at
+// decode sizes.
+#include <math.h>
+
+#include <cuda_bf16.h>
+
 #include "internal.cuh"
 
 namespace moef {
@@ -42,6 +48,112 @@ check_kernel(const int32_t *__restrict__ idx, int64_t n, int64_t P, int32_t *bad
     if ((threadIdx.x & 31) == 0 && local) atomicAdd(bad_count, static_cast<int32_t>(local));
 }
 
+// fp32 -> bf16 bits, round to nearest even (hardware conversion); a NaN
+// keeps its payload's upper bits with the quiet bit set.
+__device__ __forceinline__ uint32_t bf16_bits_rne(float w) {
+    const uint32_t u = __float_as_uint(w);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (u >> 16) | 0x0040u;
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(w)));
+}
+
+__global__ void __launch_bounds__(kThreads)
+pack_kernel(const int32_t *__restrict__ expert_ids, const float *__restrict__ weights,
+            int64_t n, int32_t *__restrict__ packed) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += stride) {
+        const uint32_t e = static_cast<uint32_t>(__ldg(expert_ids + i));
+        packed[i] = static_cast<int32_t>((e << 16) | bf16_bits_rne(__ldg(weights + i)));
+    }
+}
+
+// Top-K gate, one warp per token.  Lane l holds logits l, l+32, l+64, ...
+// (EPL of them) and keeps the best of its unselected ones.  Each of the K
+// rounds finds the warp's largest unselected logit with two single-
+// instruction warp reductions: the maximum of an order-preserving integer
+// key of the logits, then the minimum expert id among the lanes holding
+// that key (equal logits: lowest expert id first).  Only the winning lane
+// rescans its own logits.  Lane k keeps round k's winner; the weights are a
+// softmax or a normalised sigmoid over the K kept logits, reduced across
+// lanes 0..K-1.
+constexpr int kRouteWarps = 4;
+
+// Order-preserving map from fp32 to uint32 (non-NaN inputs): a larger
+// float gives a larger key, equal floats (-0 and +0 too) equal keys; every
+// key is above 0, which marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int EPL>
+__device__ __forceinline__ void lane_best(const float (&v)[EPL], uint32_t open, int lane,
+                                          uint32_t *key, int *id, float *val) {
+    *key = 0u;
+    *id = 0x7FFFFFFF;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        if ((open >> j) & 1u) {
+            const uint32_t kj = order_key(v[j]);
+            if (kj > *key) { *key = kj; *id = lane + 32 * j; *val = v[j]; }
+        }
+    }
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kind,
+                  int32_t *__restrict__ expert_ids, float *__restrict__ weights,
+                  int32_t *__restrict__ packed) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
+    if (t >= T) return;                 // whole warps leave together
+    const float *z = logits + static_cast<int64_t>(t) * E;
+    float v[EPL];
+    uint32_t open = 0;                  // bit j: slot j holds an unselected logit
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < E ? __ldg(z + e) : -INFINITY;
+        if (e < E) open |= 1u << j;
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    uint32_t bk;
+    int bi;
+    float bv = 0.f;
+    lane_best(v, open, lane, &bk, &bi, &bv);
+    float kept_v = 0.f, top = 0.f;
+    int kept_id = 0;
+    for (int k = 0; k < K; ++k) {
+        const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const uint32_t wi = __reduce_min_sync(
+            0xFFFFFFFFu, (bk == wk && bk != 0u) ? static_cast<uint32_t>(bi) : 0xFFFFFFFFu);
+        const float wv = __shfl_sync(0xFFFFFFFFu, bv, static_cast<int>(wi & 31u));
+        if (lane == k) { kept_v = wv; kept_id = static_cast<int>(wi); }
+        if (k == 0) top = wv;
+        if (static_cast<int>(wi & 31u) == lane) {     // the winner's lane rescans
+            open &= ~(1u << (wi >> 5));
+            lane_best(v, open, lane, &bk, &bi, &bv);
+        }
+    }
+    float s = 0.f;
+    if (lane < K)
+        s = (kind == MOEF_GATE_SOFTMAX) ? expf(kept_v - top) : 1.f / (1.f + expf(-kept_v));
+    float total = s;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+    if (lane < K) {
+        const float w = s / total;
+        const int64_t i = static_cast<int64_t>(t) * K + lane;
+        if (expert_ids) expert_ids[i] = kept_id;
+        if (weights) weights[i] = w;
+        if (packed)
+            packed[i] = static_cast<int32_t>((static_cast<uint32_t>(kept_id) << 16) |
+                                             bf16_bits_rne(w));
+    }
+}
+
 unsigned grid_for(int64_t n, int num_sms) {
     int64_t blocks = (n + kThreads - 1) / kThreads;
     const int64_t cap = static_cast<int64_t>(num_sms) * 4;
@@ -50,7 +162,42 @@ unsigned grid_for(int64_t n, int num_sms) {
     return static_cast<unsigned>(blocks);
 }
 
+template <int EPL>
+cudaError_t launch_route_t(const float *logits, int T, int E, int K, int kind, int32_t *ids,
+                           float *w, int32_t *packed, cudaStream_t stream) {
+    void *args[] = {&logits, &T, &E, &K, &kind, &ids, &w, &packed};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((T + kRouteWarps - 1) / kRouteWarps));
+    cfg.blockDim = dim3(kRouteWarps * 32);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&topk_route_kernel<EPL>),
+                               args);
+}
+
 }  // namespace
+
+cudaError_t launch_pack(const int32_t *expert_ids, const float *weights, int64_t n,
+                        int32_t *packed, int num_sms, cudaStream_t stream) {
+    void *args[] = {&expert_ids, &weights, &n, &packed};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(&pack_kernel),
+                            dim3(grid_for(n, num_sms)), dim3(kThreads), args, 0, stream);
+}
+
+cudaError_t launch_topk_route(const float *logits, int T, int E, int K, int kind,
+                              int32_t *expert_ids, float *weights, int32_t *packed,
+                              cudaStream_t stream) {
+    if (E <= 32) return launch_route_t<1>(logits, T, E, K, kind, expert_ids, weights, packed, stream);
+    if (E <= 64) return launch_route_t<2>(logits, T, E, K, kind, expert_ids, weights, packed, stream);
+    if (E <= 128) return launch_route_t<4>(logits, T, E, K, kind, expert_ids, weights, packed, stream);
+    if (E <= 256) return launch_route_t<8>(logits, T, E, K, kind, expert_ids, weights, packed, stream);
+    if (E <= 512) return launch_route_t<16>(logits, T, E, K, kind, expert_ids, weights, packed, stream);
+    return launch_route_t<32>(logits, T, E, K, kind, expert_ids, weights, packed, stream);
+}
 
 cudaError_t launch_unpack(const int32_t *packed, int64_t n, int32_t *expert_ids,
                           float *weights, int num_sms, cudaStream_t stream) {

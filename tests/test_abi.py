@@ -100,6 +100,21 @@ def test_argument_errors(mf):
     assert u(NULL, 4, A, A, NULL) == NUL
     assert u(A, 4, NULL, NULL, NULL) == NUL
     assert u(A + 2, 4, A, NULL, NULL) == ALIGN
+    g = mf.lib().moe_topk_route
+    assert g(A, 0, 256, 8, 0, A, NULL, NULL, NULL) == OK
+    assert g(A, 4, 256, 0, 0, A, NULL, NULL, NULL) == SHAPE
+    assert g(A, 4, 4, 8, 0, A, NULL, NULL, NULL) == SHAPE        # K > E
+    assert g(A, 4, 2048, 8, 0, A, NULL, NULL, NULL) == SHAPE     # E > 1024
+    assert g(A, 4, 256, 33, 0, A, NULL, NULL, NULL) == SHAPE
+    assert g(A, 4, 256, 8, 2, A, NULL, NULL, NULL) == ARG
+    assert g(NULL, 4, 256, 8, 0, A, NULL, NULL, NULL) == NUL
+    assert g(A, 4, 256, 8, 0, NULL, NULL, NULL, NULL) == NUL
+    assert g(A + 2, 4, 256, 8, 0, A, NULL, NULL, NULL) == ALIGN
+    pk = mf.lib().pack_topk_ids
+    assert pk(A, A, 0, A, NULL) == OK
+    assert pk(A, A, -1, A, NULL) == SHAPE
+    assert pk(NULL, A, 4, A, NULL) == NUL
+    assert pk(A, A, 4, A + 2, NULL) == ALIGN
     c = mf.lib().moe_finalize_check_indices
     assert c(A, 2, 2, 16, NULL, NULL) == NUL
     assert c(A, -1, 2, 16, A, NULL) == SHAPE
