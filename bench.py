@@ -12,8 +12,10 @@ Also reported on the same line:
     (rotating copies larger than L2), timed as CUDA-graph replays and as
     back-to-back eager calls;
   * roofline of the finalize kernel against the measured HBM copy peak;
-  * e2e: the same GB/s with host (pinned) inputs copied in and results
-    copied out inside the timed region;
+  * e2e: the same GB/s with inputs and outputs in pinned host memory,
+    through the host-buffer call (the kernel reads and writes host memory in
+    place over the host link); e2e_copy: the same with H2D copies of the
+    inputs and D2H copies of the results around a device-buffer call;
   * cpu_baseline: the fp64 CPU oracle on the host cores (test
     infrastructure, timed only here);
   * SM clocks and throttle reasons sampled during the timed region.
@@ -366,10 +368,37 @@ def gate_latency(mf, device, T, E=256, K=8, calls=2000):
     return round(statistics.median(samples), 3)
 
 
-def e2e(mf, wl, host, device, steps):
-    """GB/s with host inputs: per step, H2D of every input, the call, D2H of
-    the results, all inside the timed region."""
-    d = device_inputs(wl, device)
+def e2e_zero_copy(mf, wl, host, device, steps):
+    """GB/s with the inputs and outputs in pinned host memory, through the
+    public host-buffer call: the kernel reads the inputs and writes the
+    outputs over the host link in place (no separate copies)."""
+    outs = {k: torch.empty((wl.T, wl.H), dtype=torch.bfloat16, pin_memory=True)
+            for k in ("residual_out", "norm_out")}
+
+    def step():
+        mf.moe_finalize_host(host["x"], host["idx"], host["w"], wl.wkind, host["shared"],
+                             device=device, routed_scale=wl.routed_scale,
+                             residual=host["residual"], gamma=host["gamma"], eps=wl.eps,
+                             write_out=False, **outs)
+
+    step()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    nb = workload_bytes(wl, write_out=False)
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    return ms, nb - d2h, d2h
+
+
+def e2e_copy(mf, wl, host, device, steps):
+    """GB/s with host inputs: per step, H2D copies of every input, the call on
+    device buffers, D2H copies of the results, all inside the timed region."""
+    d = {k: v.to(device) for k, v in host.items()}
     outs = {"residual_out": torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device),
             "norm_out": torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device)}
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
@@ -392,6 +421,7 @@ def e2e(mf, wl, host, device, steps):
     b.record()
     torch.cuda.synchronize(device)
     ms = a.elapsed_time(b) / steps
+    del d, outs
     return ms, h2d, d2h
 
 
@@ -483,15 +513,18 @@ def run_ours(args, ws, rank, local):
     achieved = nbytes / (kernel_ms * 1e-3) / 1e9
     traffic = recorded_traffic()
 
-    host = {"x": host_tensor(wl.permuted_out), "idx": host_tensor(wl.idx),
-            "w": host_tensor(np.ascontiguousarray(wl.weights)), "shared": host_tensor(wl.shared),
-            "residual": host_tensor(wl.residual), "gamma": host_tensor(wl.gamma)}
+    del d, outs
+    torch.cuda.empty_cache()
+    host = {"x": host_tensor(wl.permuted_out), "idx": host_tensor(wl.idx).pin_memory(),
+            "w": host_tensor(np.ascontiguousarray(wl.weights)).pin_memory(),
+            "shared": host_tensor(wl.shared), "residual": host_tensor(wl.residual),
+            "gamma": host_tensor(wl.gamma)}
     e2e_steps = max(3, min(args.steps, 20))
-    e2e_ms, h2d, d2h = e2e(mf, wl, host, device, e2e_steps)
+    e2e_ms, h2d, d2h = e2e_zero_copy(mf, wl, host, device, e2e_steps)
     e2e_ms = max_over_ranks(e2e_ms, ws)
     e2e_value = sum_over_ranks(nbytes, ws) / (e2e_ms * 1e-3) / 1e9
-
-    del d, outs
+    c_ms, c_h2d, c_d2h = e2e_copy(mf, wl, host, device, e2e_steps)
+    c_ms = max_over_ranks(c_ms, ws)
     torch.cuda.empty_cache()
     decode = {}
     if not args.skip_decode:
@@ -531,7 +564,13 @@ def run_ours(args, ws, rank, local):
                      "peak_source": peak_src, "kernel_ms": round(kernel_ms, 5)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": round(e2e_ms, 3)},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": round(e2e_ms, 3),
+                "mode": "moe_finalize_host: pinned host inputs read and pinned host outputs "
+                        "written by the kernel over the host link, no separate copies"},
+        "e2e_copy": {"value": round(sum_over_ranks(nbytes, ws) / (c_ms * 1e-3) / 1e9, 1),
+                     "unit": "GB/s", "h2d_bytes_per_step": c_h2d, "d2h_bytes_per_step": c_d2h,
+                     "steps": e2e_steps, "ms_per_step": round(c_ms, 3),
+                     "mode": "H2D copies of all inputs, call on device buffers, D2H copies"},
         "clocks": clocks,
         "gpu_launches": args.steps,
         "decode": decode,

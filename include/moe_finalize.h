@@ -34,7 +34,12 @@
  * consumer holding only residual_out can reproduce norm_out.
  *
  * Conventions for every entry point:
- *   - all array pointers are DEVICE pointers unless stated otherwise;
+ *   - all array pointers are DEVICE pointers unless stated otherwise:
+ *     addresses the current device can load from and store to.  Page-locked
+ *     host memory (cudaHostAlloc / cudaHostRegister) qualifies under unified
+ *     addressing: the kernels then read and write host memory in place over
+ *     the host link, with no separate copies (slower than HBM, but input
+ *     reads, compute and output writes overlap);
  *     bf16 arrays are raw IEEE bfloat16 bit patterns (uint16_t storage);
  *   - all arrays are dense, row-major, with no padding between rows;
  *   - the caller owns every buffer; the library allocates no memory, never

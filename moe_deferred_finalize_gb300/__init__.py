@@ -8,10 +8,11 @@ kernels and their C ABI live in ``libmoe_finalize.so``
 (``include/moe_finalize.h``); this package is its thin Python binding.
 """
 from ._abi import (WKIND, BoundFinalize, MoefError, bind, check_indices, lib,  # noqa: F401
-                   moe_finalize, moe_finalize_unfused, moe_finalize_unfused_noalloc,
+                   moe_finalize, moe_finalize_host, moe_finalize_unfused,
+                   moe_finalize_unfused_noalloc,
                    pack_topk_ids, plan, topk_route, unfused_workspace_bytes, unpack_topk_ids)
 
-__all__ = ["moe_finalize", "bind", "BoundFinalize", "moe_finalize_unfused",
+__all__ = ["moe_finalize", "moe_finalize_host", "bind", "BoundFinalize", "moe_finalize_unfused",
            "moe_finalize_unfused_noalloc", "topk_route", "pack_topk_ids",
            "unfused_workspace_bytes", "unpack_topk_ids", "check_indices", "plan", "lib",
            "MoefError", "WKIND"]

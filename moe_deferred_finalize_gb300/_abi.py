@@ -103,7 +103,10 @@ def _stream(stream, device):
 def _check(t, name, dtypes, shape, device):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device != device:
+    if device is _PINNED:
+        if t.device.type != "cpu" or not t.is_pinned():
+            raise ValueError(f"{name} must be a pinned (page-locked) CPU tensor")
+    elif t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
     if t.dtype not in dtypes:
         raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
@@ -114,16 +117,27 @@ def _check(t, name, dtypes, shape, device):
 
 
 _BF16 = (torch.bfloat16,)
+_PINNED = object()      # "device" of host tensors read and written in place by the kernel
+
+
+def _empty(shape, device):
+    if device is _PINNED:
+        return torch.empty(shape, dtype=torch.bfloat16, pin_memory=True)
+    return torch.empty(shape, dtype=torch.bfloat16, device=device)
 
 
 def _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale, residual, gamma,
-             eps, out, residual_out, norm_out, write_out, splits, threads):
-    """Validate, allocate missing outputs; returns (C arguments, outputs)."""
+             eps, out, residual_out, norm_out, write_out, splits, threads, host=False):
+    """Validate, allocate missing outputs; returns (C arguments, outputs).
+    host=True: every tensor is a pinned CPU tensor, used in place."""
     if wkind not in WKIND:
         raise ValueError(f"wkind must be one of {sorted(WKIND)}")
-    device = permuted_out.device
-    if device.type != "cuda":
-        raise ValueError("permuted_out must be a CUDA tensor")
+    if host:
+        device = _PINNED
+    else:
+        device = permuted_out.device
+        if device.type != "cuda":
+            raise ValueError("permuted_out must be a CUDA tensor")
     if permuted_out.dim() != 2 or idx_map.dim() != 2:
         raise ValueError("permuted_out is [P, H] and idx_map is [T, K]")
     P, H = permuted_out.shape
@@ -139,16 +153,16 @@ def _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale, re
         _check(residual, "residual", _BF16, (T, H), device)
         _check(gamma, "gamma", _BF16, (H,), device)
         if residual_out is None:
-            residual_out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+            residual_out = _empty((T, H), device)
         if norm_out is None:
-            norm_out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+            norm_out = _empty((T, H), device)
         _check(residual_out, "residual_out", _BF16, (T, H), device)
         _check(norm_out, "norm_out", _BF16, (T, H), device)
     elif residual_out is not None or norm_out is not None:
         raise ValueError("residual_out / norm_out need a residual")
     if not norm or write_out:
         if out is None:
-            out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+            out = _empty((T, H), device)
         _check(out, "out", _BF16, (T, H), device)
     else:
         out = None
@@ -248,6 +262,33 @@ def moe_finalize_unfused_noalloc(permuted_out: torch.Tensor, idx_map: torch.Tens
     st = _lib().moe_finalize_unfused_noalloc(*args[:16], _stream(stream, permuted_out.device))
     if st != 0:
         raise MoefError(st, "moe_finalize_unfused_noalloc")
+    return res
+
+
+def moe_finalize_host(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: torch.Tensor,
+                      wkind: str, shared_out: torch.Tensor, *, device=None,
+                      routed_scale: float = 1.0, residual: Optional[torch.Tensor] = None,
+                      gamma: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                      out: Optional[torch.Tensor] = None,
+                      residual_out: Optional[torch.Tensor] = None,
+                      norm_out: Optional[torch.Tensor] = None, write_out: bool = True,
+                      stream=None) -> dict:
+    """The finalize on host buffers, without copies: every tensor is a
+    pinned (page-locked) CPU tensor, and the kernel on ``device`` (default:
+    the current CUDA device) reads the inputs and writes the outputs in host
+    memory directly over the host link, so input reads, compute and output
+    writes overlap.  Outputs are allocated pinned when not given.  Arguments
+    as for ``moe_finalize``; results are bit-identical to it for the same
+    launch plan.  Enqueued on the device's current stream (or ``stream``):
+    synchronise before reading the outputs."""
+    args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
+                         residual, gamma, eps, out, residual_out, norm_out, write_out, 0, 0,
+                         host=True)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    st = _lib().moe_finalize_ex(*args, _stream(stream, dev))
+    if st != 0:
+        raise MoefError(st, "moe_finalize_host")
     return res
 
 
