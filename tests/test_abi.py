@@ -174,6 +174,20 @@ def test_plan_invariants(mf):
                         assert p["cluster"] == 1
 
 
+def test_plan_size_limits(mf):
+    # the grid is T * splits CTAs and must fit a signed 32-bit count
+    assert mf.plan(2**31 // 8, 8, 7168, False)["grid"] == 2**31 // 8
+    with pytest.raises(mf.MoefError) as e:
+        mf.plan(2**31 - 1, 8, 7168, True, splits=2)
+    assert e.value.status == 2
+    # RMSNorm rows: at most 16 CTAs x 256 threads x 8 vectors of 8 values
+    assert mf.plan(1, 8, 262144, True)["cluster"] == 16
+    with pytest.raises(mf.MoefError):
+        mf.plan(1, 8, 262152, True)
+    # without RMSNorm any row length works (several passes per CTA)
+    assert mf.plan(1, 8, 8 * 2**20, False)["vpt"] == 8
+
+
 def test_plan_hints(mf):
     p = mf.plan(1, 8, 7168, False, splits=28, threads=32)
     assert (p["splits"], p["slice"], p["threads"], p["vpt"]) == (28, 32, 32, 1)

@@ -68,6 +68,20 @@ def test_random_shapes(cuda_lib, orc, T, K, H, wkind, norm):
     compare(run_gpu(cuda_lib, wl), run_oracle(orc, wl), f"T={T} K={K} H={H} {wkind}: ")
 
 
+def test_longest_rmsnorm_row(cuda_lib, orc):
+    """H = 262144 with RMSNorm: the longest row one cluster of 16 CTAs x 256
+    threads x 8 vectors can normalise; one more vector is refused."""
+    H = 16 * 256 * 8 * 8
+    wl = W.synth("long", T=2, K=4, H=H, E=64, tile=8, P=64, weight_rule="sigmoid",
+                 routed_scale=2.5, with_norm=True, seed=31, require_all=False)
+    p = cuda_lib.plan(wl.T, wl.K, H, True)
+    assert p["cluster"] == 16 and p["threads"] == 256 and p["vpt"] == 8
+    compare(run_gpu(cuda_lib, wl), run_oracle(orc, wl), "H=262144: ")
+    with pytest.raises(cuda_lib.MoefError) as e:
+        cuda_lib.plan(2, 4, H + 8, True)
+    assert e.value.status == 2
+
+
 @pytest.mark.parametrize("splits,threads", [(1, 0), (1, 256), (2, 0), (3, 64), (7, 128),
                                             (8, 0), (13, 96), (16, 0)])
 def test_launch_shapes_agree(cuda_lib, orc, splits, threads):
