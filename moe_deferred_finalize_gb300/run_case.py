@@ -4,6 +4,8 @@ For profilers: one process, a handful of launches, a known input size.
 
   python -m moe_deferred_finalize_gb300.run_case --workload decode_bs256 --iters 3
   python -m moe_deferred_finalize_gb300.run_case --prefill-tokens 4096 --iters 3
+  python -m moe_deferred_finalize_gb300.run_case --workload decode_bs1_packed --unfused
+  python -m moe_deferred_finalize_gb300.run_case --gate-tokens 16384 --iters 3
 """
 import argparse
 
@@ -26,20 +28,35 @@ def main(argv=None):
     g = ap.add_mutually_exclusive_group(required=True)
     g.add_argument("--workload", choices=W.CONFIG_NAMES)
     g.add_argument("--prefill-tokens", type=int)
+    g.add_argument("--gate-tokens", type=int,
+                   help="run the top-K gate (E=256, K=8, sigmoid, packed) on this many tokens")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--write-out", action="store_true",
                     help="with a residual, also write out (default: residual_out + norm_out only)")
+    ap.add_argument("--unfused", action="store_true", help="run the unfused A/B path")
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--threads", type=int, default=0)
     args = ap.parse_args(argv)
+    if args.gate_tokens:
+        g_ = torch.Generator(device="cuda").manual_seed(0)
+        z = torch.randn((args.gate_tokens, 256), generator=g_, device="cuda")
+        for _ in range(args.iters):
+            mf.topk_route(z, 8, "sigmoid", want_packed=True)
+        torch.cuda.synchronize()
+        print(f"gate: T={args.gate_tokens} E=256 K=8 iters={args.iters} ok")
+        return
     wl = W.make(args.workload) if args.workload else W.prefill(args.prefill_tokens)
     x, idx, w, sh = _dev(wl.permuted_out), _dev(wl.idx), _dev(wl.weights), _dev(wl.shared)
     res = _dev(wl.residual) if wl.with_norm else None
     gam = _dev(wl.gamma) if wl.with_norm else None
     for _ in range(args.iters):
-        mf.moe_finalize(x, idx, w, wl.wkind, sh, routed_scale=wl.routed_scale, residual=res,
-                        gamma=gam, eps=wl.eps, write_out=args.write_out or not wl.with_norm,
-                        splits=args.splits, threads=args.threads)
+        if args.unfused:
+            mf.moe_finalize_unfused(x, idx, w, wl.wkind, sh, routed_scale=wl.routed_scale,
+                                    residual=res, gamma=gam, eps=wl.eps)
+        else:
+            mf.moe_finalize(x, idx, w, wl.wkind, sh, routed_scale=wl.routed_scale, residual=res,
+                            gamma=gam, eps=wl.eps, write_out=args.write_out or not wl.with_norm,
+                            splits=args.splits, threads=args.threads)
     torch.cuda.synchronize()
     print(f"{wl.name}: T={wl.T} K={wl.K} H={wl.H} P={wl.P} iters={args.iters} ok")
 
