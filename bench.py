@@ -124,50 +124,66 @@ def recorded_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 10 ms with
+    timestamps; only the samples inside the timed window are summarised
+    (the nearest one after the window opened when the window is shorter
+    than the sampling period)."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, device_index):
         self.proc = None
         self.dev = device_index
+        self.window = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(self.dev), "-lms", "100"],
+                 "-i", str(self.dev), "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.5)
+
+    def mark(self, t0, t1):
+        """The timed window, in host wall-clock seconds."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.15)
+        time.sleep(0.05)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        samples = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        t0, t1 = self.window or (samples[0][0], samples[-1][0])
+        inside = [x for x in samples if t0 <= x[0] <= t1]
+        in_window = len(inside)
+        if not inside:
+            after = [x for x in samples if x[0] >= t0]
+            inside = after[:1] or samples[-1:]
+        reasons = sorted({n for x in inside for n, v in zip(self.REASONS, x[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": max(x[2] for x in inside), "samples": len(inside),
+                "samples_in_window": in_window, "window_ms": round(1e3 * (t1 - t0), 1),
+                "reasons": reasons}
 
 
 def pinned_alloc(shape, dtype):
@@ -208,7 +224,7 @@ def call(mf, wl, d, outs, stream=None):
                     write_out="out" in outs, stream=stream)
 
 
-def time_headline(mf, wl, d, outs, steps, warmup, ws, device):
+def time_headline(mf, wl, d, outs, steps, warmup, ws, device, sampler=None):
     stream = torch.cuda.current_stream(device)
     for _ in range(warmup):
         call(mf, wl, d, outs)
@@ -217,11 +233,15 @@ def time_headline(mf, wl, d, outs, steps, warmup, ws, device):
           for _ in range(steps)]
     barrier(ws)
     torch.cuda.synchronize(device)
+    t0 = time.time()
     for a, b in ev:
         a.record(stream)
         call(mf, wl, d, outs)
         b.record(stream)
     torch.cuda.synchronize(device)
+    t1 = time.time()
+    if sampler is not None:
+        sampler.mark(t0, t1)
     barrier(ws)
     per = [a.elapsed_time(b) for a, b in ev]
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
@@ -502,7 +522,8 @@ def run_ours(args, ws, rank, local):
     sampler = ClockSampler(device.index if device.index is not None else 0)
     if rank == 0:
         sampler.start()
-    total_ms, per = time_headline(mf, wl, d, outs, args.steps, args.warmup, ws, device)
+    total_ms, per = time_headline(mf, wl, d, outs, args.steps, args.warmup, ws, device,
+                                  sampler if rank == 0 else None)
     clocks = sampler.stop() if rank == 0 else None
 
     ms_step = max_over_ranks(total_ms / args.steps, ws)
