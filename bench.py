@@ -216,12 +216,12 @@ def device_inputs(wl, device):
     return d
 
 
-def call(mf, wl, d, outs, stream=None):
+def call(mf, wl, d, outs, stream=None, routing_ready=False):
     mf.moe_finalize(d["x"], d["idx"], d["w"], wl.wkind, d["shared"],
                     routed_scale=wl.routed_scale, residual=d.get("residual"),
                     gamma=d.get("gamma"), eps=wl.eps, out=outs.get("out"),
                     residual_out=outs.get("residual_out"), norm_out=outs.get("norm_out"),
-                    write_out="out" in outs, stream=stream)
+                    write_out="out" in outs, routing_ready=routing_ready, stream=stream)
 
 
 def time_headline(mf, wl, d, outs, steps, warmup, ws, device, sampler=None):
@@ -283,6 +283,10 @@ def decode_latency(mf, name, device, reps):
         for f in bound:
             f()
 
+    def one_pass_ready():     # idx/weights are not written inside the loop
+        for dd, oo in sets:
+            call(mf, wl, dd, oo, routing_ready=True)
+
     def one_pass_unfused():
         for dd, oo in sets:
             mf.moe_finalize_unfused(dd["x"], dd["idx"], dd["w"], wl.wkind, dd["shared"],
@@ -328,6 +332,7 @@ def decode_latency(mf, name, device, reps):
     eager_checked_us = eager(one_pass)      # argument checks on every call
     eager_us = eager(one_pass_bound)        # checked once, then raw C-ABI calls
     graph_us = graph(one_pass)
+    ready_us = graph(one_pass_ready)
     unfused_us = graph(one_pass_unfused)
     plan = mf.plan(wl.T, wl.K, wl.H, norm, True,
                    torch.cuda.get_device_properties(device).multi_processor_count)
@@ -335,6 +340,7 @@ def decode_latency(mf, name, device, reps):
     return {"T": wl.T, "K": wl.K, "H": wl.H, "routing": wl.wkind, "rmsnorm": norm,
             "us_per_call_graph": round(graph_us, 3), "us_per_call_eager": round(eager_us, 3),
             "us_per_call_eager_checked": round(eager_checked_us, 3),
+            "us_per_call_graph_routing_ready": round(ready_us, 3),
             "unfused_us_per_call_graph": round(unfused_us, 3),
             "GBps_graph": round(touched / (graph_us * 1e-6) / 1e9, 1),
             "copies": R, "calls": n_pass * R, "plan": plan}

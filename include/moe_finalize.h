@@ -177,9 +177,25 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok,
                               moef_plan *plan);
 
 /*
+ * Flags of moe_finalize_ex.
+ *
+ * MOEF_FLAG_ROUTING_READY: idx_map and weights were complete before the
+ * previous kernel on `stream` started (in an MoE layer they come from the
+ * routing step, while the kernel just before the finalize is the expert
+ * GEMM that writes permuted_out).  The kernel then reads them before it
+ * waits for the previous kernel, which takes one dependent memory round
+ * trip off its critical path when launches overlap.  Everything else
+ * (permuted_out, shared_out, residual, gamma, the outputs) is still touched
+ * only after the previous kernel has completed.  Do not set it when the
+ * previous kernel may write idx_map or weights.
+ */
+#define MOEF_FLAG_ROUTING_READY 1u
+
+/*
  * moe_finalize_ex -- moe_finalize with launch hints (0 = automatic), for
  * callers that pin a launch shape (e.g. one captured graph for several
- * batch sizes) and for tuning.  Same arguments and rules otherwise.
+ * batch sizes) and for tuning, and with `flags` (MOEF_FLAG_*, 0 = none;
+ * unknown bits give MOEF_ERR_ARG).  Same arguments and rules otherwise.
  */
 moef_status moe_finalize_ex(const void *permuted_out, int64_t P,
                             const int32_t *idx_map,
@@ -189,7 +205,7 @@ moef_status moe_finalize_ex(const void *permuted_out, int64_t P,
                             const void *residual, const void *gamma, float eps,
                             void *out, void *residual_out, void *norm_out,
                             int T, int K, int H,
-                            int splits_hint, int threads_hint,
+                            int splits_hint, int threads_hint, unsigned flags,
                             cudaStream_t stream);
 
 /*

@@ -56,7 +56,7 @@ def _lib():
         common = [vp, i64, vp, vp, i32, f32, vp, vp, vp, f32, vp, vp, vp, i32, i32, i32]
         lib.moe_finalize.argtypes = common + [vp]
         lib.moe_finalize.restype = i32
-        lib.moe_finalize_ex.argtypes = common + [i32, i32, vp]
+        lib.moe_finalize_ex.argtypes = common + [i32, i32, ctypes.c_uint, vp]
         lib.moe_finalize_ex.restype = i32
         lib.moe_finalize_unfused.argtypes = common + [vp, ctypes.c_size_t, vp]
         lib.moe_finalize_unfused.restype = i32
@@ -126,8 +126,12 @@ def _empty(shape, device):
     return torch.empty(shape, dtype=torch.bfloat16, device=device)
 
 
+FLAG_ROUTING_READY = 1
+
+
 def _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale, residual, gamma,
-             eps, out, residual_out, norm_out, write_out, splits, threads, host=False):
+             eps, out, residual_out, norm_out, write_out, splits, threads, host=False,
+             routing_ready=False):
     """Validate, allocate missing outputs; returns (C arguments, outputs).
     host=True: every tensor is a pinned CPU tensor, used in place."""
     if wkind not in WKIND:
@@ -168,7 +172,8 @@ def _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale, re
         out = None
     args = (_ptr(permuted_out), P, _ptr(idx_map), _ptr(weights), WKIND[wkind],
             float(routed_scale), _ptr(shared_out), _ptr(residual), _ptr(gamma), float(eps),
-            _ptr(out), _ptr(residual_out), _ptr(norm_out), T, K, H, int(splits), int(threads))
+            _ptr(out), _ptr(residual_out), _ptr(norm_out), T, K, H, int(splits), int(threads),
+            FLAG_ROUTING_READY if routing_ready else 0)
     res = {"out": out}
     if norm:
         res["residual_out"] = residual_out
@@ -182,7 +187,8 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
                  eps: float = 1e-6, out: Optional[torch.Tensor] = None,
                  residual_out: Optional[torch.Tensor] = None,
                  norm_out: Optional[torch.Tensor] = None, write_out: bool = True,
-                 splits: int = 0, threads: int = 0, stream=None) -> dict:
+                 splits: int = 0, threads: int = 0, routing_ready: bool = False,
+                 stream=None) -> dict:
     """Deferred MoE finalize on the GPU (see include/moe_finalize.h).
 
     permuted_out bf16 [P, H]; idx_map int32 [T, K]; weights [T, K] encoded
@@ -192,10 +198,12 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
     given; with a residual, ``write_out=False`` skips ``out``.  Returns a dict
     with "out" and, with a residual, "residual_out" and "norm_out".
     Enqueued on the current stream (or ``stream``); nothing is synchronised.
+    ``routing_ready``: idx_map and weights were complete before the previous
+    kernel on the stream started (MOEF_FLAG_ROUTING_READY).
     """
     args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
                          residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
-                         threads)
+                         threads, routing_ready=routing_ready)
     st = _lib().moe_finalize_ex(*args, _stream(stream, permuted_out.device))
     if st != 0:
         raise MoefError(st, "moe_finalize")
@@ -320,13 +328,13 @@ def bind(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: torch.Tenso
          eps: float = 1e-6, out: Optional[torch.Tensor] = None,
          residual_out: Optional[torch.Tensor] = None, norm_out: Optional[torch.Tensor] = None,
          write_out: bool = True, splits: int = 0, threads: int = 0,
-         stream=None) -> BoundFinalize:
+         routing_ready: bool = False, stream=None) -> BoundFinalize:
     """Check and marshal a finalize once (arguments as for ``moe_finalize``);
     the returned object enqueues it on ``stream`` (default: the current
     stream at bind time) each time it is called."""
     args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
                          residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
-                         threads)
+                         threads, routing_ready=routing_ready)
     return BoundFinalize(args, res, stream, permuted_out.device)
 
 

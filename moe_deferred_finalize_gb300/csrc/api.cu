@@ -197,6 +197,7 @@ moef_status check_finalize_args(const void *permuted_out, int64_t P, const int32
     p->T = T;
     p->K = K;
     p->H = H;
+    p->routing_ready = 0;
     return MOEF_OK;
 }
 
@@ -213,8 +214,9 @@ moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *
                             const void *shared_out, const void *residual, const void *gamma,
                             float eps, void *out, void *residual_out, void *norm_out,
                             int T, int K, int H, int splits_hint, int threads_hint,
-                            cudaStream_t stream) {
+                            unsigned flags, cudaStream_t stream) {
     if (splits_hint < 0 || threads_hint < 0) return MOEF_ERR_ARG;
+    if (flags & ~MOEF_FLAG_ROUTING_READY) return MOEF_ERR_ARG;
     moef::FinalizeParams p;
     bool vec_ok = false;
     moef_status st = check_finalize_args(permuted_out, P, idx_map, weights, wkind, routed_scale,
@@ -229,6 +231,7 @@ moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *
                            threads_hint, &plan);
     if (st != MOEF_OK) return st;
     apply_plan(plan, &p);
+    p.routing_ready = (flags & MOEF_FLAG_ROUTING_READY) ? 1 : 0;
     return moef::launch_finalize(p, plan, stream) == cudaSuccess ? MOEF_OK : MOEF_ERR_CUDA;
 }
 
@@ -273,7 +276,7 @@ moef_status moe_finalize(const void *permuted_out, int64_t P, const int32_t *idx
                          float eps, void *out, void *residual_out, void *norm_out,
                          int T, int K, int H, cudaStream_t stream) {
     return moe_finalize_ex(permuted_out, P, idx_map, weights, wkind, routed_scale, shared_out,
-                           residual, gamma, eps, out, residual_out, norm_out, T, K, H, 0, 0,
+                           residual, gamma, eps, out, residual_out, norm_out, T, K, H, 0, 0, 0u,
                            stream);
 }
 

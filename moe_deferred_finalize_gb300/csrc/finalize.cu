@@ -64,12 +64,30 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
     const int v_begin = split * p.slice;
     const int v_end = min(v_begin + p.slice, p.nvec);
 
+    // Stage the token's row pointers and scaled weights (the routed scale
+    // folded into the weight once, "Support deferred MoE finalize ...",
+    // Modifications item 2).
+    const bool stage = threadIdx.x < K;
+    int r = 0;
+    float w = 0.f;
+    const int64_t slot = static_cast<int64_t>(t) * K + threadIdx.x;
+    // The routing inputs may be read before the grid dependency wait when the
+    // caller says no earlier kernel still writes them.
+    if (p.routing_ready && stage) {
+        r = __ldg(p.idx + slot);
+        w = decode_weight(p.weights, p.wkind, slot);
+    }
+
     // Launched as a programmatic dependent of the previous kernel on the
-    // stream: nothing before this point touches global memory, so the launch
-    // and CTA set-up overlap the previous kernel's tail, and every read and
-    // write below sees it complete.
+    // stream: nothing else before this point touches global memory, so the
+    // launch and CTA set-up overlap the previous kernel's tail, and every read
+    // and write below sees it complete.
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    if (!p.routing_ready && stage) {
+        r = __ldg(p.idx + slot);
+        w = decode_weight(p.weights, p.wkind, slot);
+    }
     // This thread's first dense operands do not depend on the row map: their
     // loads go out before the staging barrier, beside the row-map loads.
     const int v_first = v_begin + threadIdx.x;
@@ -78,15 +96,9 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
         sh_first = Ops::load(p.shared + tok + static_cast<int64_t>(v_first) * VEC);
         if (NORM) rs_first = Ops::load(p.residual + tok + static_cast<int64_t>(v_first) * VEC);
     }
-
-    // Stage the token's row pointers and scaled weights (the routed scale
-    // folded into the weight once, "Support deferred MoE finalize ...",
-    // Modifications item 2).
-    if (threadIdx.x < K) {
-        const int64_t i = static_cast<int64_t>(t) * K + threadIdx.x;
-        const int r = __ldg(p.idx + i);
+    if (stage) {
         s_row[threadIdx.x] = p.x + static_cast<int64_t>(r) * p.H;
-        s_w[threadIdx.x] = decode_weight(p.weights, p.wkind, i) * p.routed_scale;
+        s_w[threadIdx.x] = w * p.routed_scale;
     }
     __syncthreads();
 

@@ -28,6 +28,7 @@ struct FinalizeParams {
     int nvec;                   // vectors per row = H / vec
     int splits;                 // CTAs per token
     int slice;                  // vectors per CTA
+    int routing_ready;          // idx/weights may be read before the grid dependency wait
 };
 
 // Launches one finalize according to `plan` (validated by the caller).

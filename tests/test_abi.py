@@ -42,6 +42,12 @@ def test_library_exports_every_declared_symbol(mf):
         assert hasattr(lib, name), name
 
 
+def test_unknown_flags_rejected(mf):
+    f = mf.lib().moe_finalize_ex
+    assert f(A, 16, A, A, 0, 1.0, A, None, None, 1e-6, A, None, None, 0, 2, 8, 0, 0, 2, None) == 4
+    assert f(A, 16, A, A, 0, 1.0, A, None, None, 1e-6, A, None, None, 0, 2, 8, 0, 0, 1, None) == 0
+
+
 def test_status_strings(mf):
     s = mf.lib().moef_status_string
     for code in range(7):

@@ -117,6 +117,19 @@ def test_norm_split_beyond_cluster_limit_is_rejected(cuda_lib):
     assert e.value.status == 4
 
 
+@pytest.mark.parametrize("name", ["decode_bs1_packed", "fused_norm_bs16", "decode_bs256"])
+def test_routing_ready_flag_same_result(cuda_lib, name):
+    """Reading the row map and weights before the grid dependency wait
+    changes no bit of the result."""
+    wl = W.make(name)
+    dev = to_device(wl)
+    a = run_gpu(cuda_lib, wl, dev)
+    b = run_gpu(cuda_lib, wl, dev, routing_ready=True)
+    for key in a:
+        if a[key] is not None:
+            assert np.array_equal(bits_of(a[key]), bits_of(b[key])), key
+
+
 def test_one_slot_weight_one_is_the_row(cuda_lib):
     wl = W.synth("k1", T=9, K=1, H=7168, E=64, tile=16, P=256, seed=21, require_all=False)
     dev = to_device(wl)
