@@ -66,13 +66,13 @@ const char *moef_status_string(moef_status s) {
 
 // Plan choice, from sweeps of T = 1..4096 at H = 7168 on GB300 (graph
 // replay, inputs larger than L2):
-//  * without RMSNorm, latency regime: while one 16-byte vector per thread
-//    fits in about two waves of fully occupied SMs, every thread takes one
-//    vector (vpt = 1) and a row is cut into 128-vector slices, one CTA each.
-//    Every gathered load of the call is then in flight at once, which is
-//    what decode batch sizes need (the time is a few memory latencies).
-//  * without RMSNorm, bandwidth regime: one CTA of 128 threads per token
-//    row, each thread up to 8 vectors.
+//  * without RMSNorm a row is cut into 128-vector slices, one CTA of 128
+//    threads each, one vector per thread, at every T: at decode sizes every
+//    gathered load of the call is then in flight at once (the time is a few
+//    memory latencies), and at large T the many small CTAs avoid the wave
+//    quantisation that whole-row CTAs hit (T = 1536: 32.1 vs 36.6 us).  When
+//    that grid would need between one and two waves, 64-thread CTAs taking
+//    two vectors each fit it in one (T = 256: 7.2 vs 7.7 us).
 //  * with RMSNorm a row must be finished by one CTA or one cluster, and
 //    cluster launches cost more the larger and the more numerous they are:
 //    rows are split into slices of at most 256 vectors (one per thread of a
@@ -105,9 +105,16 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, in
         if (splits > kMaxCluster) splits = kMaxCluster;
         if (splits == 1) threads_auto = rows < 4 * static_cast<int64_t>(num_sms) ? kMaxThreads : 128;
     } else {
-        const int64_t one_per_thread = rows * nvec;
-        const int64_t two_waves = static_cast<int64_t>(num_sms) * 2048 * 2;
-        splits = (one_per_thread <= two_waves) ? ceil_div(nvec, 128) : 1;
+        // 128-vector slices; if that grid would need between one and two
+        // waves of 128-thread CTAs (8 per SM at 64 registers), 64-thread CTAs
+        // with two vectors each fit it in one wave instead.
+        splits = ceil_div(nvec, 128);
+        if (rows * splits > 0x7FFFFFFFLL) splits = static_cast<int>(0x7FFFFFFFLL / rows);
+        if (splits < 1) splits = 1;
+        const int64_t slots128 = static_cast<int64_t>(num_sms) * 8;
+        const int64_t grid = rows * splits;
+        if (!threads_hint && grid > slots128 && grid < 2 * slots128 && nvec >= 128)
+            threads_auto = 64;
     }
     if (with_norm && splits > kMaxCluster) return MOEF_ERR_ARG;
 
@@ -117,7 +124,7 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, in
     int threads;
     if (threads_hint) {
         threads = threads_hint;
-    } else if (threads_auto && splits == 1) {
+    } else if (threads_auto) {
         threads = threads_auto;
         if (ceil_div(slice, threads) > kMaxVpt) threads = kMaxThreads;
     } else {

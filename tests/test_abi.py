@@ -140,8 +140,12 @@ def test_plan_regimes(mf):
     assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (2, 256, 2, 2)
     p = mf.plan(512, 8, 7168, True)         # one CTA per row from ~3 CTAs per SM on
     assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (1, 256, 4, 1)
-    p = mf.plan(256, 8, 7168, False)
-    assert (p["splits"], p["vpt"], p["grid"]) == (7, 1, 1792)
+    p = mf.plan(128, 8, 7168, False)
+    assert (p["splits"], p["threads"], p["vpt"], p["grid"]) == (7, 128, 1, 896)
+    p = mf.plan(256, 8, 7168, False)        # 1792 CTAs: 64-thread CTAs fit one wave
+    assert (p["splits"], p["threads"], p["vpt"], p["grid"]) == (7, 64, 2, 1792)
+    p = mf.plan(4096, 8, 7168, False)       # large T without RMSNorm: still 128-vector slices
+    assert (p["splits"], p["threads"], p["vpt"]) == (7, 128, 1)
     # bandwidth sizes: one CTA of 128 threads per token row
     p = mf.plan(16384, 8, 7168, True)
     assert (p["splits"], p["threads"], p["vpt"], p["cluster"], p["grid"]) == (1, 128, 8, 1, 16384)
@@ -182,7 +186,8 @@ def test_plan_invariants(mf):
 
 def test_plan_size_limits(mf):
     # the grid is T * splits CTAs and must fit a signed 32-bit count
-    assert mf.plan(2**31 // 8, 8, 7168, False)["grid"] == 2**31 // 8
+    p = mf.plan(2**31 // 8, 8, 7168, False)
+    assert p["grid"] == (2**31 // 8) * p["splits"] <= 2**31 - 1
     with pytest.raises(mf.MoefError) as e:
         mf.plan(2**31 - 1, 8, 7168, True, splits=2)
     assert e.value.status == 2
@@ -190,8 +195,11 @@ def test_plan_size_limits(mf):
     assert mf.plan(1, 8, 262144, True)["cluster"] == 16
     with pytest.raises(mf.MoefError):
         mf.plan(1, 8, 262152, True)
-    # without RMSNorm any row length works (several passes per CTA)
-    assert mf.plan(1, 8, 8 * 2**20, False)["vpt"] == 8
+    # without RMSNorm any row length works
+    p = mf.plan(1, 8, 8 * 2**20, False)
+    assert p["splits"] * p["slice"] * 8 >= 8 * 2**20
+    p = mf.plan(2**30, 8, 7168, False)      # grid capped: fewer, longer slices
+    assert p["grid"] <= 2**31 - 1 and p["vpt"] == 8
 
 
 def test_plan_hints(mf):
