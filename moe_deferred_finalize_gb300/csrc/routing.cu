@@ -68,14 +68,14 @@ pack_kernel(const int32_t *__restrict__ expert_ids, const float *__restrict__ we
 }
 
 // Top-K gate, one warp per token.  Lane l holds logits l, l+32, l+64, ...
-// (EPL of them) and keeps the best of its unselected ones.  Each of the K
-// rounds finds the warp's largest unselected logit with two single-
-// instruction warp reductions: the maximum of an order-preserving integer
-// key of the logits, then the minimum expert id among the lanes holding
-// that key (equal logits: lowest expert id first).  Only the winning lane
-// rescans its own logits.  Lane k keeps round k's winner; the weights are a
-// softmax or a normalised sigmoid over the K kept logits, reduced across
-// lanes 0..K-1.
+// (EPL of them), each turned once into an order-preserving 32-bit key, and
+// keeps the best of its unselected keys.  Each of the K rounds finds the
+// warp's largest unselected logit with two single-instruction warp
+// reductions: the maximum key, then the minimum expert id among the lanes
+// holding it (equal logits: lowest expert id first).  Only the winning lane
+// clears that key and rescans its own keys.  Lane k keeps round k's winner;
+// the weights are a softmax or a normalised sigmoid over the K kept logits
+// (recovered exactly from their keys), reduced across lanes 0..K-1.
 constexpr int kRouteWarps = 4;
 
 // Order-preserving map from fp32 to uint32 (non-NaN inputs): a larger
@@ -86,18 +86,19 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Best (largest) key of the lane and its slot; key 0 when none is left.
 template <int EPL>
-__device__ __forceinline__ void lane_best(const float (&v)[EPL], uint32_t open, int lane,
-                                          uint32_t *key, int *id, float *val) {
-    *key = 0u;
-    *id = 0x7FFFFFFF;
+__device__ __forceinline__ void lane_best(const uint32_t (&key)[EPL], uint32_t *best,
+                                          int *slot) {
+    *best = 0u;
+    *slot = 0;
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-        if ((open >> j) & 1u) {
-            const uint32_t kj = order_key(v[j]);
-            if (kj > *key) { *key = kj; *id = lane + 32 * j; *val = v[j]; }
-        }
-    }
+    for (int j = 0; j < EPL; ++j)
+        if (key[j] > *best) { *best = key[j]; *slot = j; }   // strict: lowest slot on ties
 }
 
 template <int EPL>
@@ -110,33 +111,33 @@ topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kin
     const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
     if (t >= T) return;                 // whole warps leave together
     const float *z = logits + static_cast<int64_t>(t) * E;
-    float v[EPL];
-    uint32_t open = 0;                  // bit j: slot j holds an unselected logit
+    uint32_t key[EPL];
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
         const int e = lane + 32 * j;
-        v[j] = e < E ? __ldg(z + e) : -INFINITY;
-        if (e < E) open |= 1u << j;
+        key[j] = e < E ? order_key(__ldg(z + e)) : 0u;
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     uint32_t bk;
-    int bi;
-    float bv = 0.f;
-    lane_best(v, open, lane, &bk, &bi, &bv);
-    float kept_v = 0.f, top = 0.f;
+    int bj;
+    lane_best(key, &bk, &bj);
+    uint32_t kept_key = 0u, top_key = 0u;
     int kept_id = 0;
     for (int k = 0; k < K; ++k) {
         const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, bk);
         const uint32_t wi = __reduce_min_sync(
-            0xFFFFFFFFu, (bk == wk && bk != 0u) ? static_cast<uint32_t>(bi) : 0xFFFFFFFFu);
-        const float wv = __shfl_sync(0xFFFFFFFFu, bv, static_cast<int>(wi & 31u));
-        if (lane == k) { kept_v = wv; kept_id = static_cast<int>(wi); }
-        if (k == 0) top = wv;
+            0xFFFFFFFFu, bk == wk ? static_cast<uint32_t>(lane + 32 * bj) : 0xFFFFFFFFu);
+        if (lane == k) { kept_key = wk; kept_id = static_cast<int>(wi); }
+        if (k == 0) top_key = wk;
         if (static_cast<int>(wi & 31u) == lane) {     // the winner's lane rescans
-            open &= ~(1u << (wi >> 5));
-            lane_best(v, open, lane, &bk, &bi, &bv);
+#pragma unroll
+            for (int j = 0; j < EPL; ++j)
+                if (j == bj) key[j] = 0u;
+            lane_best(key, &bk, &bj);
         }
     }
+    const float kept_v = key_value(kept_key);
+    const float top = key_value(top_key);
     float s = 0.f;
     if (lane < K)
         s = (kind == MOEF_GATE_SOFTMAX) ? expf(kept_v - top) : 1.f / (1.f + expf(-kept_v));
