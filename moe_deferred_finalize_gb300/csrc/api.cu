@@ -4,6 +4,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "internal.cuh"
 
 namespace {
@@ -29,20 +31,24 @@ int vpt_bucket(int need) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Multiprocessor count of the current device, cached per device.
+// Multiprocessor count of the current device, cached per device (host
+// threads may race to fill an entry; they all store the same value).
 cudaError_t current_sms(int *sms) {
-    static int cache[kMaxDevices];
+    static std::atomic<int> cache[kMaxDevices];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) {
-        *sms = cache[dev];
-        return cudaSuccess;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int cached = cache[dev].load(std::memory_order_relaxed);
+        if (cached > 0) {
+            *sms = cached;
+            return cudaSuccess;
+        }
     }
     int n = 0;
     err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < kMaxDevices) cache[dev] = n;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
     *sms = n;
     return cudaSuccess;
 }

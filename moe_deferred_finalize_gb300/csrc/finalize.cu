@@ -29,6 +29,8 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "internal.cuh"
 #include "vec.cuh"
 
@@ -212,16 +214,17 @@ cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, cudaStream_
     ++num_attrs;
     if (CLUSTER) {
         if (plan.cluster > 8) {
-            // Clusters of 9..16 CTAs are opt-in per kernel and device.
-            static int enabled[64];
+            // Clusters of 9..16 CTAs are opt-in per kernel and device (setting
+            // the attribute twice from racing host threads is harmless).
+            static std::atomic<int> enabled[64];
             int dev = 0;
             cudaError_t err = cudaGetDevice(&dev);
             if (err != cudaSuccess) return err;
-            if (dev >= 64) return cudaErrorInvalidDevice;
-            if (!enabled[dev]) {
+            if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+            if (!enabled[dev].load(std::memory_order_relaxed)) {
                 err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                 if (err != cudaSuccess) return err;
-                enabled[dev] = 1;
+                enabled[dev].store(1, std::memory_order_relaxed);
             }
         }
         attr[num_attrs].id = cudaLaunchAttributeClusterDimension;

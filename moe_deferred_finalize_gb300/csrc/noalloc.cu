@@ -19,6 +19,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "moe_finalize.h"
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MOEF_NOALLOC_SCRATCH_BYTES];
@@ -31,18 +33,18 @@ constexpr int kMaxDevices = 64;
 // Device address of g_noalloc_scratch on the current device (looked up once
 // per device; the lookup allocates nothing).
 cudaError_t scratch_address(void **out) {
-    static void *cached[kMaxDevices];
+    static std::atomic<void *> cached[kMaxDevices];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!cached[dev]) {
-        void *ptr = nullptr;
+    void *ptr = cached[dev].load(std::memory_order_relaxed);
+    if (!ptr) {
         err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (err != cudaSuccess) return err;
-        cached[dev] = ptr;
+        cached[dev].store(ptr, std::memory_order_relaxed);
     }
-    *out = cached[dev];
+    *out = ptr;
     return cudaSuccess;
 }
 
