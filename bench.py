@@ -586,6 +586,11 @@ def run_ours(args, ws, rank, local):
                    "l2": "inputs larger than L2 (%.2f GB read per step)" % (
                        (nbytes - 2 * wl.T * wl.H * 2) / 1e9),
                    "plan": plan},
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "per_call_us": ({"T1": decode["T1"]["us_per_call_graph"],
+                         "T256": decode["T256"]["us_per_call_graph"],
+                         "timing": "CUDA-graph replay of back-to-back calls, inputs rotated "
+                                   "over copies larger than L2"} if decode else None),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peak_src, "kernel_ms": round(kernel_ms, 5)},
