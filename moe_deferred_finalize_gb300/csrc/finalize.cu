@@ -21,11 +21,18 @@
 // shared memory.  With RMSNorm the bf16-rounded residual_out vectors are kept
 // in shared memory between the two passes (each thread its own column, so
 // no barrier is needed; in registers they cost 32 registers per thread and
-// halved the resident CTAs, and with them the loads in flight); the sum of
-// squares is reduced with warp
-// shuffles and shared memory, and across the CTAs of a split row through
-// distributed shared memory of a thread-block cluster (every CTA adds the
-// partials in the same order, so all slices use the same inverse RMS).
+// halved the resident CTAs, and with them the loads in flight).  The sum of
+// squares is reduced with warp shuffles and shared memory, and across the
+// CTAs of a split row through distributed shared memory of a thread-block
+// cluster (every CTA adds the partials in the same order, so all slices use
+// the same inverse RMS).
+//
+// Launch order: the kernel is a programmatic dependent of the previous
+// kernel on the stream.  It touches global memory only after
+// griddepcontrol.wait (the row map and weights may come first when the
+// caller vouches that no earlier kernel still writes them), and it lets the
+// next kernel start launching once its gathered loads are done.  No thread
+// ever spins: the only waits are barriers.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
