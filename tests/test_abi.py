@@ -211,3 +211,14 @@ def test_plan_hints(mf):
         mf.plan(1, 8, 7168, True, splits=17)
     with pytest.raises(mf.MoefError):
         mf.plan(1, 8, 7168, True, splits=1, threads=32)   # norm row needs 28 vectors/thread
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libmoe_finalize.so there is no other path: every call raises."""
+    from moe_deferred_finalize_gb300 import _abi
+    monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(_abi, "_LIB", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _abi.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        _abi.plan(1, 8, 7168, False)
