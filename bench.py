@@ -108,17 +108,26 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_code_digest():
+    """SHA-256 of the kernel sources with comments and whitespace removed:
+    it changes with the code, not with its comments."""
+    import re
+    h = hashlib.sha256()
+    for f in KERNEL_SRCS:
+        text = open(f).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("".join(text.split()).encode())
+    return h.hexdigest()
+
+
 def recorded_traffic():
-    """ncu DRAM bytes per launch recorded for the current kernel source, else None."""
+    """ncu DRAM bytes per launch recorded for the current kernel code, else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
-    h = hashlib.sha256()
-    for f in KERNEL_SRCS:
-        h.update(open(f, "rb").read())
-    sha = h.hexdigest()
-    if d.get("kernel_src_sha256") != sha or d.get("workload") != WORKLOAD:
+    if d.get("kernel_code_sha256") != kernel_code_digest() or d.get("workload") != WORKLOAD:
         return None
     return d.get("dram_bytes_per_launch")
 
