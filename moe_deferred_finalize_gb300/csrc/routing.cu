@@ -69,12 +69,14 @@ pack_kernel(const int32_t *__restrict__ expert_ids, const float *__restrict__ we
 
 // Top-K gate, one warp per token.  Lane l holds logits l, l+32, l+64, ...
 // (EPL of them), each turned once into an order-preserving 32-bit key, and
-// keeps the best of its unselected keys.  Each of the K rounds finds the
+// keeps its two best unselected keys.  Each of the K rounds finds the
 // warp's largest unselected logit with two single-instruction warp
 // reductions: the maximum key, then the minimum expert id among the lanes
-// holding it (equal logits: lowest expert id first).  Only the winning lane
-// clears that key and rescans its own keys.  Lane k keeps round k's winner;
-// the weights are a softmax or a normalised sigmoid over the K kept logits
+// holding it (equal logits: lowest expert id first).  The winning lane
+// promotes its second-best key; only a lane that wins a second time before
+// it has rescanned goes over its keys again (at E = 256, K = 8 that is about
+// one rescan per token instead of K).  Lane k keeps round k's winner; the
+// weights are a softmax or a normalised sigmoid over the K kept logits
 // (recovered exactly from their keys), reduced across lanes 0..K-1.
 constexpr int kRouteWarps = 4;
 
@@ -90,15 +92,25 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Best (largest) key of the lane and its slot; key 0 when none is left.
+// The two best untaken keys of the lane and their slots (key 0: none).  On
+// equal keys the lower slot ranks first.
 template <int EPL>
-__device__ __forceinline__ void lane_best(const uint32_t (&key)[EPL], uint32_t *best,
-                                          int *slot) {
-    *best = 0u;
-    *slot = 0;
+__device__ __forceinline__ void lane_best2(const uint32_t (&key)[EPL], uint32_t taken,
+                                           uint32_t *b1, int *j1, uint32_t *b2, int *j2) {
+    *b1 = 0u;
+    *b2 = 0u;
+    *j1 = 0;
+    *j2 = 0;
 #pragma unroll
-    for (int j = 0; j < EPL; ++j)
-        if (key[j] > *best) { *best = key[j]; *slot = j; }   // strict: lowest slot on ties
+    for (int j = 0; j < EPL; ++j) {
+        const uint32_t kj = ((taken >> j) & 1u) ? 0u : key[j];
+        if (kj > *b1) {
+            *b2 = *b1; *j2 = *j1;
+            *b1 = kj; *j1 = j;
+        } else if (kj > *b2) {
+            *b2 = kj; *j2 = j;
+        }
+    }
 }
 
 template <int EPL>
@@ -118,22 +130,29 @@ topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kin
         key[j] = e < E ? order_key(__ldg(z + e)) : 0u;
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    uint32_t bk;
-    int bj;
-    lane_best(key, &bk, &bj);
+    uint32_t taken = 0u;                // slots this lane has given up
+    uint32_t b1, b2;
+    int j1, j2;
+    lane_best2(key, taken, &b1, &j1, &b2, &j2);
+    bool second_known = true;           // b2 is the lane's true second best
     uint32_t kept_key = 0u, top_key = 0u;
     int kept_id = 0;
     for (int k = 0; k < K; ++k) {
-        const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, b1);
         const uint32_t wi = __reduce_min_sync(
-            0xFFFFFFFFu, bk == wk ? static_cast<uint32_t>(lane + 32 * bj) : 0xFFFFFFFFu);
+            0xFFFFFFFFu, b1 == wk ? static_cast<uint32_t>(lane + 32 * j1) : 0xFFFFFFFFu);
         if (lane == k) { kept_key = wk; kept_id = static_cast<int>(wi); }
         if (k == 0) top_key = wk;
-        if (static_cast<int>(wi & 31u) == lane) {     // the winner's lane rescans
-#pragma unroll
-            for (int j = 0; j < EPL; ++j)
-                if (j == bj) key[j] = 0u;
-            lane_best(key, &bk, &bj);
+        if (static_cast<int>(wi & 31u) == lane) {     // this lane's best was taken
+            taken |= 1u << j1;
+            if (second_known) {
+                b1 = b2;
+                j1 = j2;
+                second_known = false;
+            } else {
+                lane_best2(key, taken, &b1, &j1, &b2, &j2);
+                second_known = true;
+            }
         }
     }
     const float kept_v = key_value(kept_key);
