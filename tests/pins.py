@@ -347,4 +347,34 @@ def pin_pack_array_library(orc):
     assert np.array_equal((got & 0xFFFF).astype(np.uint16), ref_lo)
 
 
+
+
+def _every_bf16_weight():
+    """All finite bf16 bit patterns of magnitude <= 2^100 (products stay finite)."""
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = bf16_bits_to_f32(b)
+    keep = np.isfinite(f) & (np.abs(f) <= 2.0 ** 100)
+    return b[keep], f[keep]
+
+
+def pin_weight_decode_exhaustive(orc):
+    """With one slot, a row of ones, zero shared and scale 1, out is the
+    decoded weight itself: every finite bf16 weight, the same words packed
+    beside a range of expert ids, and their fp32 widenings."""
+    bits, vals = _every_bf16_weight()
+    T = bits.size
+    x = _bits(np.ones((1, 8)))
+    idx = np.zeros((T, 1), np.int32)
+    zero = np.zeros((T, 8), np.uint16)
+    want = np.repeat(vals.astype(np.float64)[:, None], 8, axis=1)
+    r = orc.moe_finalize(x, idx, bits.reshape(T, 1), "bf16", 1.0, zero)
+    assert np.array_equal(r["out"], want)
+    experts = (np.arange(T) % 65536).astype(np.uint32)
+    words = ((experts << 16) | bits.astype(np.uint32)).view(np.int32).reshape(T, 1)
+    r = orc.moe_finalize(x, idx, words, "packed", 1.0, zero)
+    assert np.array_equal(r["out"], want)
+    r = orc.moe_finalize(x, idx, vals.reshape(T, 1), "fp32", 1.0, zero)
+    assert np.array_equal(r["out"], want)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

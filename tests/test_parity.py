@@ -284,3 +284,35 @@ def test_error_statuses_on_device(cuda_lib):
     assert e.value.status == 4
     with pytest.raises(ValueError):
         cuda_lib.moe_finalize(dev["x"], dev["idx"], dev["w"].double(), "fp32", dev["shared"])
+
+
+@pytest.mark.parametrize("wkind", ["bf16", "packed", "fp32"])
+def test_every_bf16_weight_through_the_kernel(cuda_lib, orc, wkind):
+    """One slot, a row of ones, zero shared, scale 1: out is exactly the
+    decoded weight, for every finite bf16 pattern (bit-exact vs the oracle)."""
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = W.bf16_bits_to_f32(b)
+    keep = np.isfinite(f) & (np.abs(f) <= 2.0 ** 100)
+    bits, vals = b[keep], f[keep]
+    T = bits.size
+    if wkind == "bf16":
+        w = bf16_dev(bits.reshape(T, 1))
+        w_host = bits.reshape(T, 1)
+    elif wkind == "packed":
+        words = (((np.arange(T) % 65536).astype(np.uint32) << 16) | bits).view(np.int32)
+        w_host = words.reshape(T, 1)
+        w = torch.from_numpy(w_host).cuda()
+    else:
+        w_host = vals.reshape(T, 1)
+        w = torch.from_numpy(w_host).cuda()
+    x = W.to_bf16_bits(np.ones((1, 8)))
+    idx = np.zeros((T, 1), np.int32)
+    zero = np.zeros((T, 8), np.uint16)
+    out = cuda_lib.moe_finalize(bf16_dev(x), torch.from_numpy(idx).cuda(), w, wkind,
+                                bf16_dev(zero), routed_scale=1.0)["out"]
+    torch.cuda.synchronize()
+    got = bits_of(out)
+    want = np.where(bits == 0x8000, 0, bits).astype(np.uint16)   # -0 * 1 + 0 = +0
+    assert np.array_equal(got, np.repeat(want[:, None], 8, axis=1))
+    ref = orc.moe_finalize(x, idx, w_host, wkind, 1.0, zero)["out"]
+    assert np.array_equal(W.bf16_bits_to_f32(got).astype(np.float64), ref)
