@@ -62,7 +62,9 @@
 enum { OREF_W_FP32 = 0, OREF_W_BF16 = 1, OREF_W_PACKED = 2 };
 
 /* A bf16 value is the upper 16 bits of an IEEE binary32 value; widening
- * appends sixteen zero bits, which is exact. */
+ * appends sixteen zero bits, which is exact.  (All bf16 operands of the
+ * finalize: the permuted rows, shared output, residual and gamma of the
+ * pages above.) */
 static double bf16_to_double(uint16_t bits) {
     uint32_t u = (uint32_t)bits << 16;
     float f;
@@ -120,7 +122,10 @@ void oref_unpack_topk_ids(const int32_t *packed, int64_t n,
     }
 }
 
-/* Routing weight of one (t, k) slot, decoded exactly to double. */
+/* Routing weight of one (t, k) slot, decoded exactly to double: fp32, bf16,
+ * or the low half of a packed word ("[Deepseek V4] Keep fp32 routing
+ * weights in the mxfp4 trtllm MoE", description: the finalize exists with
+ * bf16 and with fp32 weights; packed words carry a bf16 weight). */
 static double decode_weight(const void *weights, int wkind, int64_t i) {
     if (wkind == OREF_W_FP32)
         return (double)((const float *)weights)[i];
@@ -134,7 +139,9 @@ static double decode_weight(const void *weights, int wkind, int64_t i) {
 }
 
 /* RMSNorm of T rows of H values given in double:
- * y = x / sqrt(mean(x^2) + eps) * gamma. */
+ * y = x / sqrt(mean(x^2) + eps) * gamma  ("[Kimi K2.5] Fuse deferred MoE
+ * finalize into next-layer AR + residual + RMSNorm", Summary: RMSNorm of the
+ * residual sum; the standard form is the reading taken). */
 static void rmsnorm_rows_double(const double *x, const uint16_t *gamma, double eps,
                                 int64_t T, int64_t H, double *y) {
     for (int64_t t = 0; t < T; ++t) {
@@ -147,8 +154,8 @@ static void rmsnorm_rows_double(const double *x, const uint16_t *gamma, double e
     }
 }
 
-/* RMSNorm of T rows of bf16 values; used to check a norm against the
- * residual a device actually emitted. */
+/* RMSNorm of T rows of bf16 values (same definition and source as above);
+ * used to check a norm against the residual a device actually emitted. */
 void oref_rmsnorm_bf16(const uint16_t *x, const uint16_t *gamma, double eps,
                        int64_t T, int64_t H, double *y) {
     for (int64_t t = 0; t < T; ++t) {
@@ -163,7 +170,10 @@ void oref_rmsnorm_bf16(const uint16_t *x, const uint16_t *gamma, double eps,
     }
 }
 
-/* The deferred finalize, see the header comment for the definition.
+/* The deferred finalize ("Support deferred MoE finalize for MXFP4 and FP8
+ * block-scale", Motivation and Modifications item 2; "[Kimi K2.5] Fuse
+ * deferred MoE finalize ...", Summary and Key modifications); see the file
+ * comment for the definition.
  *
  * permuted_out  bf16 bits [P, H]   unweighted expert rows, padded per expert
  * idx           int32 [T, K]       row of permuted_out for slot (t, k)

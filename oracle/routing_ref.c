@@ -29,13 +29,17 @@ int32_t oref_pack_topk_id(int32_t expert_id, float weight);   /* finalize_ref.c 
 
 enum { OREF_GATE_SOFTMAX = 0, OREF_GATE_SIGMOID = 1 };
 
-/* n packed words from n (expert id, fp32 weight) pairs. */
+/* n packed words from n (expert id, fp32 weight) pairs: the packing launch
+ * of "[Deepseek V4] Keep fp32 routing weights in the mxfp4 trtllm MoE"
+ * (description), one word per pair. */
 void oref_pack_topk_ids(const int32_t *expert_ids, const float *weights, int64_t n,
                         int32_t *packed) {
     for (int64_t i = 0; i < n; ++i) packed[i] = oref_pack_topk_id(expert_ids[i], weights[i]);
 }
 
-/* Top-K routing of T tokens over E experts.  logits: fp32 [T, E];
+/* Top-K routing of T tokens over E experts, the gate named (not defined) in
+ * "[Deepseek V4] Keep fp32 routing weights ..." (description); selection
+ * and weighting follow the readings in the file comment.  logits: fp32 [T, E];
  * expert_ids: int32 [T, K] (descending logit, ties lowest id first);
  * weights: double [T, K].  Returns 0, or -1 for bad sizes or kind. */
 int oref_topk_route(const float *logits, int64_t T, int E, int K, int kind,
