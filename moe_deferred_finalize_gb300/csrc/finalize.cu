@@ -47,6 +47,7 @@ namespace moef {
 namespace {
 
 constexpr int kMaxThreads = 256;
+constexpr int kMaxClusterCtas = 16;
 
 template <int VPT, int VEC, bool NORM, bool CLUSTER>
 __global__ void __launch_bounds__(kMaxThreads)
@@ -57,11 +58,16 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
     __shared__ const uint16_t *s_row[MOEF_MAX_K];
     __shared__ float s_w[MOEF_MAX_K];
     __shared__ float s_warp[kMaxThreads / 32];
-    __shared__ float s_cta;
+    __shared__ float s_part[kMaxClusterCtas];   // partial sums of the cluster's CTAs
     // With RMSNorm: the bf16 residual_out vectors of this CTA's slice, kept
     // for the second pass ([VPT][blockDim.x], each thread its own column).
     extern __shared__ __align__(16) unsigned char s_dyn[];
     V *s_keep = reinterpret_cast<V *>(s_dyn);
+
+    // Cluster CTAs write into each other's shared memory below, which is
+    // only allowed once every CTA of the cluster has started: announce it now
+    // (non-blocking) and wait for the others just before the first remote write.
+    if constexpr (CLUSTER) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     const int S = p.splits;
     const int t = blockIdx.x / S;
@@ -184,14 +190,19 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
         for (int w = 0; w < nw; ++w) total += s_warp[w];
 
         if constexpr (CLUSTER) {
+            // Push this CTA's partial into slot [own rank] of every CTA of the
+            // cluster (thread r writes to CTA r), then one cluster barrier
+            // (release/acquire) makes all S partials visible locally.  No CTA
+            // touches another's shared memory after the barrier, so each may
+            // leave when done.
             cg::cluster_group cluster = cg::this_cluster();
-            if (threadIdx.x == 0) s_cta = total;
+            const unsigned own = cluster.block_rank();
+            asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // all CTAs started
+            if (threadIdx.x < static_cast<unsigned>(S))
+                *cluster.map_shared_rank(&s_part[own], static_cast<int>(threadIdx.x)) = total;
             cluster.sync();
             total = 0.f;
-            for (int r = 0; r < S; ++r) total += *cluster.map_shared_rank(&s_cta, r);
-            // No CTA may leave while another still reads its s_cta: arrive
-            // now, wait after the stores below.
-            asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+            for (int r = 0; r < S; ++r) total += s_part[r];    // same order in every CTA
         }
 
         const float inv = rsqrtf(total / static_cast<float>(p.H) + p.eps);
@@ -207,7 +218,6 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
                 Ops::store(p.norm_out + tok + static_cast<int64_t>(v) * VEC, Ops::from_f32(sf));
             }
         }
-        if constexpr (CLUSTER) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     }
 }
 
