@@ -79,12 +79,13 @@ const char *moef_status_string(moef_status s) {
 //    quantisation that whole-row CTAs hit (T = 1536: 32.1 vs 36.6 us).  When
 //    that grid would need between one and two waves, 64-thread CTAs taking
 //    two vectors each fit it in one (T = 256: 7.2 vs 7.7 us).
-//  * with RMSNorm a row must be finished by one CTA or one cluster, and
-//    cluster launches cost more the larger and the more numerous they are:
-//    rows are split into slices of at most 256 vectors (one per thread of a
-//    256-thread CTA) only while the grid stays under about 3 CTAs per SM;
-//    from there on one CTA takes a whole row (256 threads below 4 rows per
-//    SM, then 128).  At T = 512 this is 1.5x faster than 7-CTA clusters.
+//  * with RMSNorm a row must be finished by one CTA or one cluster.  Rows
+//    start as slices of at most 256 vectors (one per thread of a 256-thread
+//    CTA, 4-CTA clusters at H = 7168), and the split is halved while the
+//    grid exceeds about 3.5 CTAs per SM (the best grids measured held
+//    384-512 CTAs); with no split one CTA takes a whole row (256 threads
+//    below 4 rows per SM, then 128).  7-CTA clusters at T = 512 were 1.5x
+//    slower than this.
 // A row with RMSNorm must fit one pass of one CTA (256 x 8 vectors) or one
 // cluster of at most 16 such CTAs.
 moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, int num_sms,
@@ -105,8 +106,8 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, in
     } else if (with_norm) {
         const int row_fit = ceil_div(nvec, kMaxThreads * kMaxVpt);
         splits = ceil_div(nvec, kMaxThreads);
-        const int by_grid = ceil_div(3 * static_cast<int64_t>(num_sms), rows);
-        if (splits > by_grid) splits = by_grid;
+        const int64_t cap = 7 * static_cast<int64_t>(num_sms) / 2;
+        while (splits > row_fit && splits > 1 && rows * splits > cap) splits = ceil_div(splits, 2);
         if (splits < row_fit) splits = row_fit;
         if (splits > kMaxCluster) splits = kMaxCluster;
         if (splits == 1) threads_auto = rows < 4 * static_cast<int64_t>(num_sms) ? kMaxThreads : 128;

@@ -138,8 +138,14 @@ def test_plan_regimes(mf):
     assert (p["splits"], p["threads"], p["vpt"], p["cluster"], p["grid"]) == (4, 224, 1, 4, 64)
     p = mf.plan(256, 8, 7168, True)
     assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (2, 256, 2, 2)
-    p = mf.plan(512, 8, 7168, True)         # one CTA per row from ~3 CTAs per SM on
+    p = mf.plan(512, 8, 7168, True)         # one CTA per row from ~3.5 CTAs per SM on
     assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (1, 256, 4, 1)
+    p = mf.plan(192, 8, 7168, True)         # 4-CTA clusters would make 768 CTAs: halve
+    assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (2, 256, 2, 2)
+    p = mf.plan(384, 8, 7168, True)
+    assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (1, 256, 4, 1)
+    p = mf.plan(128, 8, 7168, True)
+    assert (p["splits"], p["cluster"]) == (4, 4)
     p = mf.plan(128, 8, 7168, False)
     assert (p["splits"], p["threads"], p["vpt"], p["grid"]) == (7, 128, 1, 896)
     p = mf.plan(256, 8, 7168, False)        # 1792 CTAs: 64-thread CTAs fit one wave
