@@ -54,6 +54,9 @@ CASES = [
     (40, 2, 24576, "fp32", True),      # bandwidth regime, norm row over 2 CTAs
     (33, 5, 40000, "bf16", False),     # several passes per slice without norm
     (9, 4, 4098, "fp32", True),        # H % 8 == 2: scalar path with cluster
+    (2048, 8, 4096, "fp32", True),     # bandwidth regime, other hidden sizes
+    (1500, 6, 5120, "bf16", True),
+    (1200, 9, 8192, "packed", False),
 ]
 
 
