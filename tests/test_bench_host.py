@@ -1,0 +1,77 @@
+"""bench.py host logic without a GPU: algorithmic byte counts, the clock
+sampler's window filtering and throttle-reason parsing, and the traffic
+record's comment-insensitive key."""
+import os
+import shutil
+
+import pytest
+
+import bench
+
+
+def test_algorithmic_bytes_match_the_stated_figures():
+    # T=16384, K=8, H=7168, fp32 weights, residual + RMSNorm, out not written
+    assert bench.algorithmic_bytes(16384, 8, 7168, 4, True, False) == 2_819_635_200
+    # ... with out written too
+    assert bench.algorithmic_bytes(16384, 8, 7168, 4, True, True) == 2_819_635_200 + 16384 * 7168 * 2
+    # T=256 decode, fp32 weights, out written
+    assert bench.algorithmic_bytes(256, 8, 7168, 4, False, True) == 36_716_544
+    # T=1, packed (4-byte) weights: 8 rows + shared + out + idx/words
+    assert bench.algorithmic_bytes(1, 8, 7168, 4, False, True) == 8 * 14336 + 2 * 14336 + 64
+
+
+class _FakeProc:
+    def __init__(self, text):
+        self.text = text
+
+    def terminate(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.text, ""
+
+
+def _line(ts, sm, reasons=("Not Active",) * 4):
+    return f"{ts}, {sm}, 2070, 900.0, 0x0, " + ", ".join(reasons)
+
+
+def test_clock_sampler_keeps_only_the_timed_window():
+    import datetime
+    base = datetime.datetime(2026, 1, 1, 12, 0, 0)
+    stamp = lambda s: (base + datetime.timedelta(seconds=s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    lines = [_line(stamp(0.00), 1200), _line(stamp(0.10), 2070), _line(stamp(0.20), 2070),
+             _line(stamp(0.30), 2070, ("Not Active", "Not Active", "Not Active", "Active")),
+             _line(stamp(0.40), 900)]
+    s = bench.ClockSampler(0)
+    s.proc = _FakeProc("\n".join(lines) + "\n")
+    s.mark(base.timestamp() + 0.05, base.timestamp() + 0.35)
+    r = s.stop()
+    assert r["samples_in_window"] == 3 and r["sm_mhz"] == 2070.0
+    assert r["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_short_window_takes_the_next_sample():
+    import datetime
+    base = datetime.datetime(2026, 1, 1, 12, 0, 0)
+    stamp = lambda s: (base + datetime.timedelta(seconds=s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    s = bench.ClockSampler(0)
+    s.proc = _FakeProc(_line(stamp(0.0), 1000) + "\n" + _line(stamp(0.012), 2070) + "\n")
+    s.mark(base.timestamp() + 0.004, base.timestamp() + 0.006)
+    r = s.stop()
+    assert r["samples_in_window"] == 0 and r["samples"] == 1 and r["sm_mhz"] == 2070.0
+
+
+def test_traffic_key_ignores_comments_not_code(tmp_path, monkeypatch):
+    srcs = []
+    for f in bench.KERNEL_SRCS:
+        dst = tmp_path / os.path.basename(f)
+        shutil.copy(f, dst)
+        srcs.append(str(dst))
+    monkeypatch.setattr(bench, "KERNEL_SRCS", srcs)
+    d0 = bench.kernel_code_digest()
+    with open(srcs[0], "a") as fh:
+        fh.write("\n// a new comment\n/* and a block\n   comment */\n")
+    assert bench.kernel_code_digest() == d0
+    with open(srcs[0], "a") as fh:
+        fh.write("\nstatic int changed_code = 1;\n")
+    assert bench.kernel_code_digest() != d0
