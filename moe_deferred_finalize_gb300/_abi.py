@@ -86,6 +86,21 @@ def lib():
     return _lib()
 
 
+_FAST = False
+
+
+def _fastcall():
+    """The _fastcall extension (bound-call replay) if it was built, else None."""
+    global _FAST
+    if _FAST is False:
+        try:
+            from . import _fastcall as fast
+        except ImportError:
+            fast = None
+        _FAST = fast
+    return _FAST
+
+
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -314,9 +329,23 @@ class BoundFinalize:
         self._args = args
         self._stream = _stream(stream, device)
         self.outputs = res
+        self._packed = None
+        fast = _fastcall()
+        if fast is not None:
+            # the same arguments packed once into a C struct: each call then
+            # passes only the stream to moe_finalize_ex
+            fn = ctypes.cast(self._fn, ctypes.c_void_p).value
+            vals = [a.value if isinstance(a, ctypes.c_void_p) else a for a in args]
+            self._packed = fast.pack(fn, *vals)
+            self._call = fast.call
+            self._stream_int = self._stream.value or 0
 
     def __call__(self, stream=None):
-        st = self._fn(*self._args, self._stream if stream is None else _stream(stream, None))
+        if self._packed is not None:
+            s = self._stream_int if stream is None else (_stream(stream, None).value or 0)
+            st = self._call(self._packed, s)
+        else:
+            st = self._fn(*self._args, self._stream if stream is None else _stream(stream, None))
         if st != 0:
             raise MoefError(st, "moe_finalize")
         return self.outputs

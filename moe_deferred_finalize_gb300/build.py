@@ -44,6 +44,7 @@ def _stale():
 def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile (if needed) and return the path of libmoe_finalize.so."""
     if not force and not _stale():
+        build_fastcall()
         return LIB
     os.makedirs(OBJ_DIR, exist_ok=True)
     nvcc = _nvcc()
@@ -67,7 +68,31 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    build_fastcall()
     return LIB
+
+
+FASTCALL_SRC = os.path.join(CSRC, "fastcall.c")
+
+
+def build_fastcall() -> str:
+    """Compile the _fastcall CPython extension (bound-call replay, no CUDA
+    code) next to the library; returns its path, or "" when the Python
+    headers are not available (the binding then uses ctypes for every call)."""
+    import sysconfig
+    inc = sysconfig.get_paths()["include"]
+    out = os.path.join(PKG, "_fastcall" + sysconfig.get_config_var("EXT_SUFFIX"))
+    if not os.path.exists(os.path.join(inc, "Python.h")):
+        return ""
+    if os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(FASTCALL_SRC):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    r = subprocess.run(["gcc", "-O2", "-shared", "-fPIC", "-Wall", "-I", inc, "-o", tmp,
+                        FASTCALL_SRC], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"gcc failed on fastcall.c:\n{r.stderr}")
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -228,3 +228,34 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         _abi.lib()
     with pytest.raises(RuntimeError, match="not built"):
         _abi.plan(1, 8, 7168, False)
+
+
+def test_fastcall_packs_arguments_in_abi_order(mf):
+    """The packed replay of bind() passes each argument to the same position
+    as ctypes does: every error below is triggered by one argument alone."""
+    from moe_deferred_finalize_gb300 import _abi
+    fast = _abi._fastcall()
+    if fast is None:
+        pytest.skip("_fastcall not built (no Python headers)")
+    lib = mf.lib()
+    fn = ctypes.cast(lib.moe_finalize_ex, ctypes.c_void_p).value
+    base = dict(x=A, P=16, idx=A, w=A, wkind=0, scale=1.0, shared=A, residual=None,
+                gamma=None, eps=1e-6, out=A, residual_out=None, norm_out=None, T=2, K=2, H=8,
+                splits=0, threads=0, flags=0)
+    order = list(base)
+    cases = [dict(T=0), dict(x=None), dict(idx=None), dict(w=None), dict(shared=None),
+             dict(out=None), dict(residual=A), dict(gamma=A), dict(residual_out=A),
+             dict(norm_out=A), dict(wkind=3), dict(K=33), dict(H=0), dict(P=0), dict(x=A + 1),
+             dict(out=A + 1), dict(idx=A + 2), dict(w=A + 2), dict(splits=-1),
+             dict(flags=2), dict(residual=A, gamma=A, residual_out=A, norm_out=A, eps=-1.0)]
+    seen = set()
+    for c in cases:
+        a = {**base, **c}
+        vals = [a[k] for k in order]
+        st_ctypes = lib.moe_finalize_ex(*vals, None)
+        st_fast = fast.call(fast.pack(fn, *vals), 0)
+        assert st_fast == st_ctypes, (c, st_fast, st_ctypes)
+        seen.add(st_ctypes)
+    assert seen == {0, 1, 2, 3, 4}
+    with pytest.raises(ValueError):
+        fast.pack(0, *[base[k] for k in order])

@@ -319,3 +319,34 @@ def test_every_bf16_weight_through_the_kernel(cuda_lib, orc, wkind):
     assert np.array_equal(got, np.repeat(want[:, None], 8, axis=1))
     ref = orc.moe_finalize(x, idx, w_host, wkind, 1.0, zero)["out"]
     assert np.array_equal(W.bf16_bits_to_f32(got).astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("name", ["decode_bs1_packed", "fused_norm_bs16"])
+def test_bound_call_matches_direct_call(cuda_lib, name):
+    """bind() (packed C-struct replay when built) gives the direct call's bits,
+    on the bound stream and on another stream, with and without routing_ready."""
+    wl = W.make(name)
+    dev = to_device(wl)
+    ref = run_gpu(cuda_lib, wl, dev)
+    for ready in (False, True):
+        f = cuda_lib.bind(dev["x"], dev["idx"], dev["w"], wl.wkind, dev["shared"],
+                          routed_scale=wl.routed_scale, residual=dev.get("residual"),
+                          gamma=dev.get("gamma"), eps=wl.eps, routing_ready=ready)
+        for t in f.outputs.values():
+            if t is not None:
+                t.zero_()
+        f()
+        torch.cuda.synchronize()
+        for key in ref:
+            if ref[key] is not None:
+                assert np.array_equal(bits_of(f.outputs[key]), bits_of(ref[key])), key
+        s = torch.cuda.Stream()
+        for t in f.outputs.values():
+            if t is not None:
+                t.zero_()
+        torch.cuda.synchronize()
+        f(stream=s)
+        s.synchronize()
+        for key in ref:
+            if ref[key] is not None:
+                assert np.array_equal(bits_of(f.outputs[key]), bits_of(ref[key])), key
