@@ -1,6 +1,6 @@
-"""bench.py host logic without a GPU: algorithmic byte counts, the clock
-sampler's window filtering and throttle-reason parsing, and the traffic
-record's comment-insensitive key."""
+"""bench.py host logic without a GPU: algorithmic byte counts, the CPU
+baselines, the clock sampler's window filtering and throttle-reason
+parsing, and the traffic record's comment-insensitive key."""
 import os
 import shutil
 
@@ -75,3 +75,14 @@ def test_traffic_key_ignores_comments_not_code(tmp_path, monkeypatch):
     with open(srcs[0], "a") as fh:
         fh.write("\nstatic int changed_code = 1;\n")
     assert bench.kernel_code_digest() != d0
+
+
+def test_cpu_baselines_time_the_oracle_on_every_token():
+    from moe_deferred_finalize_gb300 import workloads as W
+    import numpy as np
+    wl = W.make("fused_norm_bs16")
+    gbps, sec, passes = bench.oracle_gbps(wl, np.arange(wl.T))
+    assert gbps > 0 and sec > 0 and passes >= 1
+    pg, psec, ppasses, threads = bench.oracle_gbps_parallel(wl)
+    assert pg > 0 and psec > 0 and ppasses >= 1
+    assert threads == len(os.sched_getaffinity(0))
