@@ -310,12 +310,15 @@ def decode_latency(mf, name, device, reps):
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def eager(fn):
-        a.record()
-        for _ in range(n_pass):
-            fn()
-        b.record()
-        torch.cuda.synchronize(device)
-        return a.elapsed_time(b) * 1e3 / (n_pass * R)
+        samples = []
+        for _ in range(5):
+            a.record()
+            for _ in range(n_pass):
+                fn()
+            b.record()
+            torch.cuda.synchronize(device)
+            samples.append(a.elapsed_time(b) * 1e3 / (n_pass * R))
+        return statistics.median(samples)
 
     def graph(fn):
         g = torch.cuda.CUDAGraph()
