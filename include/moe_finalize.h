@@ -50,7 +50,9 @@
  *   - kernels never trap: an index outside [0, P) is a contract violation
  *     (undefined results), detectable beforehand with
  *     moe_finalize_check_indices;
- *   - MOEF_ERR_CUDA means the CUDA runtime refused a launch or a query.
+ *   - MOEF_ERR_CUDA means the CUDA runtime refused a launch or a query; that
+ *     error is then taken out of the runtime's per-thread last-error slot
+ *     (cudaGetLastError), so the status is its only report.
  */
 #ifndef MOE_FINALIZE_H_
 #define MOE_FINALIZE_H_

@@ -53,6 +53,15 @@ cudaError_t current_sms(int *sms) {
     return cudaSuccess;
 }
 
+// Status of a runtime call.  A refused call also leaves its error in the
+// thread's last-error slot, where the caller's next unrelated launch check
+// would find it; the error is reported here, so it is taken out of the slot.
+moef_status cuda_status(cudaError_t err) {
+    if (err == cudaSuccess) return MOEF_OK;
+    (void)cudaGetLastError();
+    return MOEF_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -239,14 +248,15 @@ moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *
     if (st != MOEF_OK || T == 0) return st;
 
     int sms = 0;
-    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
+    st = cuda_status(current_sms(&sms));
+    if (st != MOEF_OK) return st;
     moef_plan plan;
     st = moe_finalize_plan(T, K, H, residual ? 1 : 0, vec_ok ? 1 : 0, sms, splits_hint,
                            threads_hint, &plan);
     if (st != MOEF_OK) return st;
     apply_plan(plan, &p);
     p.routing_ready = (flags & MOEF_FLAG_ROUTING_READY) ? 1 : 0;
-    return moef::launch_finalize(p, plan, stream) == cudaSuccess ? MOEF_OK : MOEF_ERR_CUDA;
+    return cuda_status(moef::launch_finalize(p, plan, stream));
 }
 
 size_t moe_finalize_unfused_workspace_bytes(int T, int H) {
@@ -273,15 +283,14 @@ moef_status moe_finalize_unfused(const void *permuted_out, int64_t P, const int3
     if (!aligned(workspace, 16)) vec_ok = false;
 
     int sms = 0;
-    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
+    st = cuda_status(current_sms(&sms));
+    if (st != MOEF_OK) return st;
     moef_plan plan;
     st = moe_finalize_plan(T, K, H, 0, vec_ok ? 1 : 0, sms, 0, 0, &plan);
     if (st != MOEF_OK) return st;
     apply_plan(plan, &p);
-    return moef::launch_unfused(p, plan, static_cast<uint16_t *>(workspace), sms, stream) ==
-                   cudaSuccess
-               ? MOEF_OK
-               : MOEF_ERR_CUDA;
+    return cuda_status(
+        moef::launch_unfused(p, plan, static_cast<uint16_t *>(workspace), sms, stream));
 }
 
 moef_status moe_finalize(const void *permuted_out, int64_t P, const int32_t *idx_map,
@@ -305,10 +314,8 @@ moef_status moe_topk_route(const float *logits, int T, int E, int K, moef_gate_k
     if (!aligned(logits, 4) || (expert_ids && !aligned(expert_ids, 4)) ||
         (weights && !aligned(weights, 4)) || (packed && !aligned(packed, 4)))
         return MOEF_ERR_ALIGN;
-    return moef::launch_topk_route(logits, T, E, K, static_cast<int>(kind), expert_ids, weights,
-                                   packed, stream) == cudaSuccess
-               ? MOEF_OK
-               : MOEF_ERR_CUDA;
+    return cuda_status(moef::launch_topk_route(logits, T, E, K, static_cast<int>(kind), expert_ids,
+                                               weights, packed, stream));
 }
 
 moef_status pack_topk_ids(const int32_t *expert_ids, const float *weights, int64_t n,
@@ -319,10 +326,9 @@ moef_status pack_topk_ids(const int32_t *expert_ids, const float *weights, int64
     if (!aligned(expert_ids, 4) || !aligned(weights, 4) || !aligned(packed, 4))
         return MOEF_ERR_ALIGN;
     int sms = 0;
-    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
-    return moef::launch_pack(expert_ids, weights, n, packed, sms, stream) == cudaSuccess
-               ? MOEF_OK
-               : MOEF_ERR_CUDA;
+    moef_status st = cuda_status(current_sms(&sms));
+    if (st != MOEF_OK) return st;
+    return cuda_status(moef::launch_pack(expert_ids, weights, n, packed, sms, stream));
 }
 
 moef_status unpack_topk_ids(const int32_t *packed, int64_t n, int32_t *expert_ids,
@@ -334,10 +340,9 @@ moef_status unpack_topk_ids(const int32_t *packed, int64_t n, int32_t *expert_id
         (weights_f32 && !aligned(weights_f32, 4)))
         return MOEF_ERR_ALIGN;
     int sms = 0;
-    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
-    return moef::launch_unpack(packed, n, expert_ids, weights_f32, sms, stream) == cudaSuccess
-               ? MOEF_OK
-               : MOEF_ERR_CUDA;
+    moef_status st = cuda_status(current_sms(&sms));
+    if (st != MOEF_OK) return st;
+    return cuda_status(moef::launch_unpack(packed, n, expert_ids, weights_f32, sms, stream));
 }
 
 moef_status moe_finalize_check_indices(const int32_t *idx_map, int T, int K, int64_t P,
@@ -348,10 +353,9 @@ moef_status moe_finalize_check_indices(const int32_t *idx_map, int T, int K, int
     if (n > 0 && !idx_map) return MOEF_ERR_NULL;
     if (!aligned(d_bad_count, 4) || (idx_map && !aligned(idx_map, 4))) return MOEF_ERR_ALIGN;
     int sms = 0;
-    if (current_sms(&sms) != cudaSuccess) return MOEF_ERR_CUDA;
-    return moef::launch_check_indices(idx_map, n, P, d_bad_count, sms, stream) == cudaSuccess
-               ? MOEF_OK
-               : MOEF_ERR_CUDA;
+    moef_status st = cuda_status(current_sms(&sms));
+    if (st != MOEF_OK) return st;
+    return cuda_status(moef::launch_check_indices(idx_map, n, P, d_bad_count, sms, stream));
 }
 
 }  // extern "C"

@@ -67,7 +67,10 @@ moef_status moe_finalize_unfused_noalloc(const void *permuted_out, int64_t P,
                                     shared_out, residual, gamma, eps, out, residual_out,
                                     norm_out, T, K, H, nullptr, 0, stream);
     void *scratch = nullptr;
-    if (scratch_address(&scratch) != cudaSuccess) return MOEF_ERR_CUDA;
+    if (scratch_address(&scratch) != cudaSuccess) {
+        (void)cudaGetLastError();   // reported by the status, not left for the next launch
+        return MOEF_ERR_CUDA;
+    }
     return moe_finalize_unfused(permuted_out, P, idx_map, weights, wkind, routed_scale,
                                 shared_out, residual, gamma, eps, out, residual_out, norm_out,
                                 T, K, H, scratch, kNoallocScratchBytes, stream);
