@@ -256,7 +256,7 @@ moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *
     if (st != MOEF_OK) return st;
     apply_plan(plan, &p);
     p.routing_ready = (flags & MOEF_FLAG_ROUTING_READY) ? 1 : 0;
-    return cuda_status(moef::launch_finalize(p, plan, stream));
+    return cuda_status(moef::launch_finalize(p, plan, sms, stream));
 }
 
 size_t moe_finalize_unfused_workspace_bytes(int T, int H) {

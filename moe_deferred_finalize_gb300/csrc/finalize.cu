@@ -27,6 +27,15 @@
 // cluster (every CTA adds the partials in the same order, so all slices use
 // the same inverse RMS).
 //
+// Two builds of every launch shape: one for the common top-8 routing, with
+// K fixed at compile time, and one for any K.  With K fixed the compiler
+// needs 40-56 registers instead of 64, so more CTAs fit an SM, which pays
+// once the grid exceeds one CTA per SM (about 1 % at T >= 256).  On grids of
+// at most one CTA per SM the time is a chain of memory latencies, and there
+// the any-K build, which issues all of a vector's K row loads before its
+// first FMA, is faster (T=1: 2.37 vs 2.68 us).  Both sum the K terms in the
+// same order, so their results are bit-identical.
+//
 // Launch order: the kernel is a programmatic dependent of the previous
 // kernel on the stream.  It touches global memory only after
 // griddepcontrol.wait (the row map and weights may come first when the
@@ -49,7 +58,8 @@ namespace {
 constexpr int kMaxThreads = 256;
 constexpr int kMaxClusterCtas = 16;
 
-template <int VPT, int VEC, bool NORM, bool CLUSTER>
+// KC: the slot count K when fixed at compile time, else 0 (K from p.K).
+template <int VPT, int VEC, bool NORM, bool CLUSTER, int KC>
 __global__ void __launch_bounds__(kMaxThreads)
 finalize_kernel(const __grid_constant__ FinalizeParams p) {
     using Ops = VecOps<VEC>;
@@ -72,7 +82,7 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
     const int S = p.splits;
     const int t = blockIdx.x / S;
     const int split = blockIdx.x - t * S;
-    const int K = p.K;
+    const int K = KC ? KC : p.K;
     const int nt = blockDim.x;
 
     const int64_t tok = static_cast<int64_t>(t) * p.H;
@@ -221,9 +231,14 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
     }
 }
 
+constexpr int kFixedK = 8;
+
 template <int VPT, int VEC, bool NORM, bool CLUSTER>
-cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, cudaStream_t stream) {
-    auto kern = finalize_kernel<VPT, VEC, NORM, CLUSTER>;
+cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, int num_sms,
+                     cudaStream_t stream) {
+    const int fixed_k = (p.K == kFixedK && plan.grid > num_sms) ? 1 : 0;
+    auto kern = fixed_k ? finalize_kernel<VPT, VEC, NORM, CLUSTER, kFixedK>
+                        : finalize_kernel<VPT, VEC, NORM, CLUSTER, 0>;
     cudaLaunchAttribute attr[2];
     unsigned num_attrs = 0;
     attr[num_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -233,15 +248,16 @@ cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, cudaStream_
         if (plan.cluster > 8) {
             // Clusters of 9..16 CTAs are opt-in per kernel and device (setting
             // the attribute twice from racing host threads is harmless).
-            static std::atomic<int> enabled[64];
+            static std::atomic<int> enabled[2][64];
             int dev = 0;
             cudaError_t err = cudaGetDevice(&dev);
             if (err != cudaSuccess) return err;
             if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-            if (!enabled[dev].load(std::memory_order_relaxed)) {
+            std::atomic<int> &done = enabled[fixed_k][dev];
+            if (!done.load(std::memory_order_relaxed)) {
                 err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                 if (err != cudaSuccess) return err;
-                enabled[dev].store(1, std::memory_order_relaxed);
+                done.store(1, std::memory_order_relaxed);
             }
         }
         attr[num_attrs].id = cudaLaunchAttributeClusterDimension;
@@ -262,28 +278,31 @@ cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, cudaStream_
 }
 
 template <int VPT, int VEC>
-cudaError_t launch_v(const FinalizeParams &p, const moef_plan &plan, cudaStream_t stream) {
-    if (!p.residual) return launch_t<VPT, VEC, false, false>(p, plan, stream);
-    if (plan.cluster > 1) return launch_t<VPT, VEC, true, true>(p, plan, stream);
-    return launch_t<VPT, VEC, true, false>(p, plan, stream);
+cudaError_t launch_v(const FinalizeParams &p, const moef_plan &plan, int num_sms,
+                     cudaStream_t stream) {
+    if (!p.residual) return launch_t<VPT, VEC, false, false>(p, plan, num_sms, stream);
+    if (plan.cluster > 1) return launch_t<VPT, VEC, true, true>(p, plan, num_sms, stream);
+    return launch_t<VPT, VEC, true, false>(p, plan, num_sms, stream);
 }
 
 template <int VEC>
-cudaError_t launch_vec(const FinalizeParams &p, const moef_plan &plan, cudaStream_t stream) {
+cudaError_t launch_vec(const FinalizeParams &p, const moef_plan &plan, int num_sms,
+                       cudaStream_t stream) {
     switch (plan.vpt) {
-        case 1: return launch_v<1, VEC>(p, plan, stream);
-        case 2: return launch_v<2, VEC>(p, plan, stream);
-        case 4: return launch_v<4, VEC>(p, plan, stream);
-        case 8: return launch_v<8, VEC>(p, plan, stream);
+        case 1: return launch_v<1, VEC>(p, plan, num_sms, stream);
+        case 2: return launch_v<2, VEC>(p, plan, num_sms, stream);
+        case 4: return launch_v<4, VEC>(p, plan, num_sms, stream);
+        case 8: return launch_v<8, VEC>(p, plan, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan, cudaStream_t stream) {
-    if (plan.vec == 8) return launch_vec<8>(p, plan, stream);
-    if (plan.vec == 1) return launch_vec<1>(p, plan, stream);
+cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan, int num_sms,
+                            cudaStream_t stream) {
+    if (plan.vec == 8) return launch_vec<8>(p, plan, num_sms, stream);
+    if (plan.vec == 1) return launch_vec<1>(p, plan, num_sms, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -31,8 +31,9 @@ struct FinalizeParams {
     int routing_ready;          // idx/weights may be read before the grid dependency wait
 };
 
-// Launches one finalize according to `plan` (validated by the caller).
-cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan,
+// Launches one finalize according to `plan` (validated by the caller) on a
+// device with `num_sms` multiprocessors.
+cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan, int num_sms,
                             cudaStream_t stream);
 
 // Launches the unfused three-kernel finalize (combine into tmp, add the

@@ -5,6 +5,7 @@ Bit-exact where the arithmetic leaves no choice (one slot of weight 1,
 zero weights, identical tokens, launch shape changes for out/residual_out).
 """
 import ctypes
+import dataclasses
 
 import numpy as np
 import pytest
@@ -110,6 +111,38 @@ def test_launch_shapes_agree_without_norm(cuda_lib, orc, splits, threads):
     res = run_gpu(cuda_lib, wl, dev, splits=splits, threads=threads)
     compare(res, run_oracle(orc, wl), f"splits={splits} threads={threads}: ")
     assert np.array_equal(bits_of(res["out"]), bits_of(base["out"]))
+
+
+@pytest.mark.parametrize("norm,splits,threads", [
+    (False, 1, 128), (False, 2, 128), (False, 4, 128), (False, 7, 128), (False, 1, 32),
+    (True, 1, 128), (True, 1, 256), (True, 2, 256), (True, 4, 224), (True, 16, 64)])
+def test_fixed_k_and_any_k_builds_agree(cuda_lib, orc, norm, splits, threads):
+    """With K = 8 a grid of more than one CTA per SM runs the build with K
+    fixed at compile time, a smaller grid the any-K build.  The first tokens
+    of a large batch, finalized alone in the same launch shape, go through
+    the other build: every output must be bit-identical (same per-element
+    arithmetic and order), and the large batch must match the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    t_small = max(1, sms // splits)
+    t_large = sms + 8
+    assert t_small * splits <= sms < t_large * splits
+    wl = W.synth("builds", T=t_large, K=8, H=7168, E=256, tile=64, P=64 * 96,
+                 weight_rule="sigmoid", routed_scale=2.5, with_norm=norm, seed=splits * 7 + norm,
+                 require_all=False)
+    small = dataclasses.replace(
+        wl, T=t_small, idx=wl.idx[:t_small], expert_ids=wl.expert_ids[:t_small],
+        weights_f32=wl.weights_f32[:t_small], weights=wl.weights[:t_small],
+        shared=wl.shared[:t_small], residual=None if wl.residual is None else wl.residual[:t_small])
+    plan_large = cuda_lib.plan(t_large, 8, 7168, norm, splits=splits, threads=threads)
+    plan_small = cuda_lib.plan(t_small, 8, 7168, norm, splits=splits, threads=threads)
+    assert {k: v for k, v in plan_large.items() if k != "grid"} == \
+           {k: v for k, v in plan_small.items() if k != "grid"}
+    big = run_gpu(cuda_lib, wl, splits=splits, threads=threads)
+    compare(big, run_oracle(orc, wl), f"T={t_large} splits={splits} threads={threads}: ")
+    sub = run_gpu(cuda_lib, small, splits=splits, threads=threads)
+    for key in ("out", "residual_out", "norm_out"):
+        if sub.get(key) is not None:
+            assert np.array_equal(bits_of(sub[key]), bits_of(big[key][:t_small])), key
 
 
 def test_norm_split_beyond_cluster_limit_is_rejected(cuda_lib):
