@@ -7,6 +7,7 @@ and calls fail loudly when the library has not been built.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -115,6 +116,14 @@ def _stream(stream, device):
     return ctypes.c_void_p(int(stream))
 
 
+def _on(device):
+    """Make ``device`` the current CUDA device for the duration of a call:
+    the library enqueues on the calling thread's current device."""
+    if device.index is None or device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def _check(t, name, dtypes, shape, device):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -219,7 +228,8 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
     args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
                          residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
                          threads, routing_ready=routing_ready)
-    st = _lib().moe_finalize_ex(*args, _stream(stream, permuted_out.device))
+    with _on(permuted_out.device):
+        st = _lib().moe_finalize_ex(*args, _stream(stream, permuted_out.device))
     if st != 0:
         raise MoefError(st, "moe_finalize")
     return res
@@ -251,8 +261,9 @@ def moe_finalize_unfused(permuted_out: torch.Tensor, idx_map: torch.Tensor,
     if workspace.device != permuted_out.device or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor on the same device")
     nbytes = workspace.numel() * workspace.element_size()
-    st = _lib().moe_finalize_unfused(*args[:16], _ptr(workspace), nbytes,
-                                     _stream(stream, permuted_out.device))
+    with _on(permuted_out.device):
+        st = _lib().moe_finalize_unfused(*args[:16], _ptr(workspace), nbytes,
+                                         _stream(stream, permuted_out.device))
     if st != 0:
         raise MoefError(st, "moe_finalize_unfused")
     return res
@@ -282,7 +293,9 @@ def moe_finalize_unfused_noalloc(permuted_out: torch.Tensor, idx_map: torch.Tens
         raise ValueError("with a residual, residual_out and norm_out must be given")
     args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
                          residual, gamma, eps, out, residual_out, norm_out, True, 0, 0)
-    st = _lib().moe_finalize_unfused_noalloc(*args[:16], _stream(stream, permuted_out.device))
+    with _on(permuted_out.device):
+        st = _lib().moe_finalize_unfused_noalloc(*args[:16],
+                                                 _stream(stream, permuted_out.device))
     if st != 0:
         raise MoefError(st, "moe_finalize_unfused_noalloc")
     return res
@@ -309,7 +322,8 @@ def moe_finalize_host(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights
                          host=True)
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
         else torch.device(device)
-    st = _lib().moe_finalize_ex(*args, _stream(stream, dev))
+    with _on(dev):
+        st = _lib().moe_finalize_ex(*args, _stream(stream, dev))
     if st != 0:
         raise MoefError(st, "moe_finalize_host")
     return res
@@ -321,7 +335,8 @@ class BoundFinalize:
     Calling it enqueues the same finalize again (same buffers, new contents
     allowed) with no per-call Python checks: the decode-loop form of
     ``moe_finalize``.  The tensors passed to ``bind`` must stay alive and
-    keep their storage while the object is used.
+    keep their storage while the object is used, and their device must be
+    the current CUDA device when the object is called (no per-call switch).
     """
 
     def __init__(self, args, res, stream, device):
@@ -401,9 +416,10 @@ def topk_route(logits: torch.Tensor, K: int, kind: str = "sigmoid", *,
         res["weights"] = torch.empty((T, K), dtype=torch.float32, device=dev)
     if want_packed:
         res["packed"] = torch.empty((T, K), dtype=torch.int32, device=dev)
-    st = _lib().moe_topk_route(_ptr(logits), T, E, int(K), GATE[kind], _ptr(res.get("expert_ids")),
-                               _ptr(res.get("weights")), _ptr(res.get("packed")),
-                               _stream(stream, dev))
+    with _on(dev):
+        st = _lib().moe_topk_route(_ptr(logits), T, E, int(K), GATE[kind],
+                                   _ptr(res.get("expert_ids")), _ptr(res.get("weights")),
+                                   _ptr(res.get("packed")), _stream(stream, dev))
     if st != 0:
         raise MoefError(st, "moe_topk_route")
     return res
@@ -418,8 +434,9 @@ def pack_topk_ids(expert_ids: torch.Tensor, weights: torch.Tensor,
     if packed is None:
         packed = torch.empty_like(expert_ids)
     _check(packed, "packed", (torch.int32,), expert_ids.shape, dev)
-    st = _lib().pack_topk_ids(_ptr(expert_ids), _ptr(weights), expert_ids.numel(), _ptr(packed),
-                              _stream(stream, dev))
+    with _on(dev):
+        st = _lib().pack_topk_ids(_ptr(expert_ids), _ptr(weights), expert_ids.numel(),
+                                  _ptr(packed), _stream(stream, dev))
     if st != 0:
         raise MoefError(st, "pack_topk_ids")
     return packed
@@ -437,8 +454,9 @@ def unpack_topk_ids(packed: torch.Tensor, expert_ids: Optional[torch.Tensor] = N
         weights = torch.empty(packed.shape, dtype=torch.float32, device=device)
     _check(expert_ids, "expert_ids", (torch.int32,), packed.shape, device)
     _check(weights, "weights", (torch.float32,), packed.shape, device)
-    st = _lib().unpack_topk_ids(_ptr(packed), packed.numel(), _ptr(expert_ids), _ptr(weights),
-                                _stream(stream, device))
+    with _on(device):
+        st = _lib().unpack_topk_ids(_ptr(packed), packed.numel(), _ptr(expert_ids),
+                                    _ptr(weights), _stream(stream, device))
     if st != 0:
         raise MoefError(st, "unpack_topk_ids")
     return expert_ids, weights
@@ -454,8 +472,9 @@ def check_indices(idx_map: torch.Tensor, P: int, counter: Optional[torch.Tensor]
     if counter is None:
         counter = torch.empty(1, dtype=torch.int32, device=device)
     T, K = idx_map.shape
-    st = _lib().moe_finalize_check_indices(_ptr(idx_map), T, K, int(P), _ptr(counter),
-                                           _stream(stream, device))
+    with _on(device):
+        st = _lib().moe_finalize_check_indices(_ptr(idx_map), T, K, int(P), _ptr(counter),
+                                               _stream(stream, device))
     if st != 0:
         raise MoefError(st, "moe_finalize_check_indices")
     return counter

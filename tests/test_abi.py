@@ -259,3 +259,16 @@ def test_fastcall_packs_arguments_in_abi_order(mf):
     assert seen == {0, 1, 2, 3, 4}
     with pytest.raises(ValueError):
         fast.pack(0, *[base[k] for k in order])
+
+
+def test_calls_switch_to_the_tensors_device(monkeypatch):
+    """The library enqueues on the calling thread's current CUDA device, so
+    the binding makes the tensors' device current around each call."""
+    import contextlib
+    import torch
+    from moe_deferred_finalize_gb300 import _abi
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    assert isinstance(_abi._on(torch.device("cuda", 0)), contextlib.nullcontext)
+    assert isinstance(_abi._on(torch.device("cuda")), contextlib.nullcontext)
+    guard = _abi._on(torch.device("cuda", 1))
+    assert isinstance(guard, torch.cuda.device) and guard.idx == 1
