@@ -45,6 +45,9 @@
  *   - the caller owns every buffer; the library allocates no memory, never
  *     synchronises the device or the stream, and keeps no per-call state;
  *     work is enqueued on `stream` and the call returns at once;
+ *   - kernels run on the calling thread's current CUDA device (the device
+ *     of the context current on the thread); `stream` must belong to it
+ *     (0 = its legacy default stream);
  *   - argument errors are detected on the host before anything is enqueued
  *     and returned as a status; nothing is launched then;
  *   - kernels never trap: an index outside [0, P) is a contract violation
