@@ -103,17 +103,42 @@ def _fastcall():
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream, device):
+# The current stream's raw handle for a device index, without building a
+# torch.cuda.Stream object (a tenth of the host time of current_stream()).
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device) -> int:
+    """cudaStream_t handle (an int) for a call on ``device``: ``stream`` if
+    given (torch.cuda.Stream, ctypes.c_void_p or int), else the device's
+    current stream."""
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+        if _RAW_STREAM is not None and device is not None and device.index is not None:
+            return _RAW_STREAM(device.index)
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, ctypes.c_void_p):
-        return stream
+        return stream.value or 0
     if isinstance(stream, torch.cuda.Stream):
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
+
+
+_EX_ADDRESS = None
+
+
+def _call_ex(args, stream: int) -> int:
+    """One moe_finalize_ex call: through the _fastcall extension when it was
+    built (direct argument conversion), else through ctypes."""
+    global _EX_ADDRESS
+    fast = _fastcall()
+    if fast is not None:
+        if _EX_ADDRESS is None:
+            _EX_ADDRESS = ctypes.cast(_lib().moe_finalize_ex, ctypes.c_void_p).value
+        return fast.call_now(_EX_ADDRESS, *args, stream)
+    return _lib().moe_finalize_ex(*args, stream)
 
 
 def _on(device):
@@ -128,13 +153,13 @@ def _check(t, name, dtypes, shape, device):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if device is _PINNED:
-        if t.device.type != "cpu" or not t.is_pinned():
+        if t.is_cuda or not t.is_pinned():
             raise ValueError(f"{name} must be a pinned (page-locked) CPU tensor")
-    elif t.device != device:
-        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    elif not t.is_cuda or t.get_device() != device.index:
+        raise ValueError(f"{name} is on {t.device}, expected a CUDA tensor on {device}")
     if t.dtype not in dtypes:
         raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -228,8 +253,9 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
     args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
                          residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
                          threads, routing_ready=routing_ready)
-    with _on(permuted_out.device):
-        st = _lib().moe_finalize_ex(*args, _stream(stream, permuted_out.device))
+    device = permuted_out.device
+    with _on(device):
+        st = _call_ex(args, _stream(stream, device))
     if st != 0:
         raise MoefError(st, "moe_finalize")
     return res
@@ -323,7 +349,7 @@ def moe_finalize_host(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
         else torch.device(device)
     with _on(dev):
-        st = _lib().moe_finalize_ex(*args, _stream(stream, dev))
+        st = _call_ex(args, _stream(stream, dev))
     if st != 0:
         raise MoefError(st, "moe_finalize_host")
     return res
@@ -350,17 +376,15 @@ class BoundFinalize:
             # the same arguments packed once into a C struct: each call then
             # passes only the stream to moe_finalize_ex
             fn = ctypes.cast(self._fn, ctypes.c_void_p).value
-            vals = [a.value if isinstance(a, ctypes.c_void_p) else a for a in args]
-            self._packed = fast.pack(fn, *vals)
+            self._packed = fast.pack(fn, *args)
             self._call = fast.call
-            self._stream_int = self._stream.value or 0
 
     def __call__(self, stream=None):
+        s = self._stream if stream is None else _stream(stream, None)
         if self._packed is not None:
-            s = self._stream_int if stream is None else (_stream(stream, None).value or 0)
             st = self._call(self._packed, s)
         else:
-            st = self._fn(*self._args, self._stream if stream is None else _stream(stream, None))
+            st = self._fn(*self._args, s)
         if st != 0:
             raise MoefError(st, "moe_finalize")
         return self.outputs
@@ -428,6 +452,8 @@ def topk_route(logits: torch.Tensor, K: int, kind: str = "sigmoid", *,
 def pack_topk_ids(expert_ids: torch.Tensor, weights: torch.Tensor,
                   packed: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """(expert_id << 16) | bf16_rne(weight) words, same shape as the inputs."""
+    if not isinstance(expert_ids, torch.Tensor) or not expert_ids.is_cuda:
+        raise ValueError("expert_ids must be a CUDA tensor")
     dev = expert_ids.device
     _check(expert_ids, "expert_ids", (torch.int32,), expert_ids.shape, dev)
     _check(weights, "weights", (torch.float32,), expert_ids.shape, dev)

@@ -231,8 +231,9 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 
 def test_fastcall_packs_arguments_in_abi_order(mf):
-    """The packed replay of bind() passes each argument to the same position
-    as ctypes does: every error below is triggered by one argument alone."""
+    """The extension's packed replay (bind()) and direct call (moe_finalize)
+    pass each argument to the same position as ctypes does: every error
+    below is triggered by one argument alone."""
     from moe_deferred_finalize_gb300 import _abi
     fast = _abi._fastcall()
     if fast is None:
@@ -255,10 +256,14 @@ def test_fastcall_packs_arguments_in_abi_order(mf):
         st_ctypes = lib.moe_finalize_ex(*vals, None)
         st_fast = fast.call(fast.pack(fn, *vals), 0)
         assert st_fast == st_ctypes, (c, st_fast, st_ctypes)
+        st_now = fast.call_now(fn, *vals, 0)
+        assert st_now == st_ctypes, (c, st_now, st_ctypes)
         seen.add(st_ctypes)
     assert seen == {0, 1, 2, 3, 4}
     with pytest.raises(ValueError):
         fast.pack(0, *[base[k] for k in order])
+    with pytest.raises(TypeError):
+        fast.call_now(fn, *[base[k] for k in order])     # the stream is missing
 
 
 def test_calls_switch_to_the_tensors_device(monkeypatch):
