@@ -169,10 +169,11 @@ _BF16 = (torch.bfloat16,)
 _PINNED = object()      # "device" of host tensors read and written in place by the kernel
 
 
-def _empty(shape, device):
+def _empty_like(t, device):
+    """An uninitialised bf16 tensor shaped like the checked [T, H] tensor t."""
     if device is _PINNED:
-        return torch.empty(shape, dtype=torch.bfloat16, pin_memory=True)
-    return torch.empty(shape, dtype=torch.bfloat16, device=device)
+        return torch.empty(t.shape, dtype=torch.bfloat16, pin_memory=True)
+    return torch.empty_like(t)
 
 
 FLAG_ROUTING_READY = 1
@@ -206,16 +207,16 @@ def _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale, re
         _check(residual, "residual", _BF16, (T, H), device)
         _check(gamma, "gamma", _BF16, (H,), device)
         if residual_out is None:
-            residual_out = _empty((T, H), device)
+            residual_out = _empty_like(shared_out, device)
         if norm_out is None:
-            norm_out = _empty((T, H), device)
+            norm_out = _empty_like(shared_out, device)
         _check(residual_out, "residual_out", _BF16, (T, H), device)
         _check(norm_out, "norm_out", _BF16, (T, H), device)
     elif residual_out is not None or norm_out is not None:
         raise ValueError("residual_out / norm_out need a residual")
     if not norm or write_out:
         if out is None:
-            out = _empty((T, H), device)
+            out = _empty_like(shared_out, device)
         _check(out, "out", _BF16, (T, H), device)
     else:
         out = None
