@@ -205,6 +205,83 @@ def test_slot_order_and_duplicates(cuda_lib, orc):
         assert np.array_equal(b[5], b[2]), key
 
 
+def test_row_offsets_beyond_2_to_the_31_elements(cuda_lib, orc):
+    """permuted_out of 300,000 rows x 7168 (4.3 GB, 2.15e9 elements): the
+    referenced rows lie past element 2^31, so row offsets must be computed in
+    64 bits.  The oracle sees a compact copy of just those rows."""
+    H, P, T, K = 7168, 300_000, 6, 8
+    rng = np.random.default_rng(11)
+    rows = np.sort(rng.choice(np.arange(P - 400, P), T * K, replace=False))
+    assert rows.min() * H > 2 ** 31
+    x = torch.empty((P, H), dtype=torch.bfloat16, device="cuda")
+    vals = W.to_bf16_bits(rng.standard_normal((T * K, H)))
+    x[torch.from_numpy(rows).cuda()] = bf16_dev(vals)
+    perm = rng.permutation(T * K)
+    idx = rows[perm].reshape(T, K).astype(np.int32)
+    w = rng.random((T, K)).astype(np.float32)
+    shared = W.to_bf16_bits(rng.standard_normal((T, H)))
+    for norm in (False, True):
+        kw = {}
+        residual = gamma = None
+        if norm:
+            residual = W.to_bf16_bits(2 * rng.standard_normal((T, H)))
+            gamma = W.to_bf16_bits(rng.uniform(0.5, 1.5, H))
+            kw = dict(residual=bf16_dev(residual), gamma=bf16_dev(gamma))
+        res = cuda_lib.moe_finalize(x, torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                                    "fp32", bf16_dev(shared), routed_scale=2.5, eps=1e-6, **kw)
+        torch.cuda.synchronize()
+        ref = orc.moe_finalize(vals, perm.reshape(T, K).astype(np.int32), w, "fp32", 2.5,
+                               shared, residual, gamma, 1e-6)
+        compare(res, ref, f"rows past 2^31 elements, norm={norm}: ")
+    del x
+    torch.cuda.empty_cache()
+
+
+def test_token_offsets_beyond_2_to_the_31_elements(cuda_lib, orc):
+    """300,000 tokens x 7168 (each dense operand 4.3 GB): token offsets into
+    shared_out, residual and the outputs pass element 2^31.  The dense inputs
+    are zero except on sampled tokens, which are checked against the oracle;
+    every other row must equal the weighted sum of its gathered rows."""
+    H, P, T, K = 7168, 64, 300_000, 2
+    rng = np.random.default_rng(12)
+    x_host = W.to_bf16_bits(rng.standard_normal((P, H)))
+    idx = rng.integers(0, P, (T, K)).astype(np.int32)
+    w = rng.random((T, K)).astype(np.float32)
+    samp = np.array([0, 1, 149_999, 299_592, 299_593, T - 2, T - 1])
+    assert samp[-1] * H > 2 ** 31
+    sh_s = W.to_bf16_bits(rng.standard_normal((len(samp), H)))
+    rs_s = W.to_bf16_bits(2 * rng.standard_normal((len(samp), H)))
+    gamma = W.to_bf16_bits(rng.uniform(0.5, 1.5, H))
+    sel = torch.from_numpy(samp).cuda()
+    x = bf16_dev(x_host)
+    idx_d, w_d = torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+    for norm in (False, True):
+        shared = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+        shared[sel] = bf16_dev(sh_s)
+        kw = {}
+        if norm:
+            residual = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+            residual[sel] = bf16_dev(rs_s)
+            kw = dict(residual=residual, gamma=bf16_dev(gamma))
+        res = cuda_lib.moe_finalize(x, idx_d, w_d, "fp32", shared, routed_scale=2.5, eps=1e-6,
+                                    **kw)
+        torch.cuda.synchronize()
+        ref = orc.moe_finalize(x_host, idx[samp], w[samp], "fp32", 2.5, sh_s,
+                               rs_s if norm else None, gamma if norm else None, 1e-6)
+        compare({k: v.index_select(0, sel) for k, v in res.items() if v is not None}, ref,
+                f"tokens past 2^31 elements, norm={norm}: ")
+        # the other rows: routed sum only (zero shared / residual), in bf16
+        routed = (w_d[:, :1] * 2.5 * x.float()[idx_d[:, 0]] +
+                  w_d[:, 1:] * 2.5 * x.float()[idx_d[:, 1]])
+        out = res["residual_out"] if norm else res["out"]
+        keep = torch.ones(T, dtype=torch.bool, device="cuda")
+        keep[sel] = False
+        diff = (out.float() - routed)[keep].abs()
+        assert (diff <= 2.0 ** -7 * routed[keep].abs() + 2e-3).all()
+        del shared, res, routed, out, diff, kw
+        torch.cuda.empty_cache()
+
+
 def test_padding_never_read(cuda_lib):
     wl = W.make("decode_bs256")
     x = wl.permuted_out.copy()
