@@ -486,36 +486,44 @@ def oracle_gbps(wl, tokens, repeat_until_s=0.0):
     return nbytes * passes / el / 1e9, el / passes, passes
 
 
-def oracle_gbps_parallel(wl, repeat_until_s=0.0):
-    """The same oracle call on token chunks from a thread per host core.
+def oracle_times(wl, want_out, reps=3):
+    """Median seconds of one oracle pass over every token of ``wl``: on one
+    thread, and as token blocks from one thread per host core.
 
     The oracle is unchanged: each thread calls it on a contiguous block of
     tokens (ctypes releases the GIL for the duration of the C call).  Returns
-    (GB/s, seconds per pass, passes, threads)."""
+    (seconds on one thread, seconds on all cores, threads)."""
     import oracle   # test infrastructure: timed here, never used by the GPU path
     from concurrent.futures import ThreadPoolExecutor
     orc = oracle.default()
+    w = np.ascontiguousarray(wl.weights)
+
+    def run(a, b):
+        orc.moe_finalize(wl.permuted_out, wl.idx[a:b], w[a:b], wl.wkind, wl.routed_scale,
+                         wl.shared[a:b], None if wl.residual is None else wl.residual[a:b],
+                         wl.gamma, wl.eps, want_out=want_out)
+
+    single = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        run(0, wl.T)
+        single.append(time.perf_counter() - t0)
     threads = max(1, len(os.sched_getaffinity(0)))
     bounds = np.linspace(0, wl.T, 4 * threads + 1).astype(int)
     chunks = [(a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
-    w = np.ascontiguousarray(wl.weights)
-
-    def one(ab):
-        a, b = ab
-        orc.moe_finalize(wl.permuted_out, wl.idx[a:b], w[a:b], wl.wkind, wl.routed_scale,
-                         wl.shared[a:b], None if wl.residual is None else wl.residual[a:b],
-                         wl.gamma, wl.eps, want_out=False)
-
-    passes, t0 = 0, time.perf_counter()
+    parallel = []
     with ThreadPoolExecutor(threads) as pool:
-        while True:
-            list(pool.map(one, chunks))
-            passes += 1
-            el = time.perf_counter() - t0
-            if el >= repeat_until_s or passes >= 3:
-                break
-    nbytes = algorithmic_bytes(wl.T, wl.K, wl.H, 4, wl.with_norm, False)
-    return nbytes * passes / el / 1e9, el / passes, passes, threads
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            list(pool.map(lambda ab: run(*ab), chunks))
+            parallel.append(time.perf_counter() - t0)
+    return statistics.median(single), statistics.median(parallel), threads
+
+
+# Which outputs each workload writes in the benchmark (the prefill emits
+# residual_out and norm_out only; every other workload writes out as well).
+def writes_out(name, wl):
+    return name != WORKLOAD or not wl.with_norm
 
 
 # ------------------------------------------------------------------- main
@@ -601,7 +609,8 @@ def run_ours(args, ws, rank, local):
     if not args.skip_decode:
         decode = {"T1": decode_latency(mf, "decode_bs1_packed", device, 4000),
                   "T256": decode_latency(mf, "decode_bs256", device, 2000),
-                  "T16_rmsnorm": decode_latency(mf, "fused_norm_bs16", device, 2000)}
+                  "T16_rmsnorm": decode_latency(mf, "fused_norm_bs16", device, 2000),
+                  "T4_tiny": decode_latency(mf, "tiny", device, 2000)}
 
     gate = {}
     if not args.skip_decode:
@@ -611,14 +620,25 @@ def run_ours(args, ws, rank, local):
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
-        gbps, sec, passes = oracle_gbps(wl, np.arange(wl.T), repeat_until_s=10.0)
-        cpu = {"value": round(gbps, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"all {wl.T} tokens of {WORKLOAD}, {passes} pass(es), "
+        sec, psec, nthr = oracle_times(wl, want_out=False)
+        cpu = {"value": round(nbytes / sec / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"all {wl.T} tokens of {WORKLOAD}, median of 3 passes, "
                          f"{sec:.2f} s per pass, single-threaded fp64"}
-        pg, psec, ppasses, nthr = oracle_gbps_parallel(wl, repeat_until_s=3.0)
-        cpu["all_cores"] = {"value": round(pg, 4), "unit": "GB/s", "cores": nthr,
-                            "sample": f"all {wl.T} tokens, {ppasses} pass(es), {psec:.2f} s "
+        cpu["all_cores"] = {"value": round(nbytes / psec / 1e9, 4), "unit": "GB/s",
+                            "cores": nthr,
+                            "sample": f"all {wl.T} tokens, median of 3 passes, {psec:.3f} s "
                                       f"per pass, token blocks on {nthr} threads"}
+        # every other workload, whole, for the per-workload table
+        cpu["workloads_ms"] = {WORKLOAD: {"one_thread": round(1e3 * sec, 3),
+                                          "all_cores": round(1e3 * psec, 3)}}
+        for name in W.CONFIG_NAMES:
+            if name == WORKLOAD:
+                continue
+            cw = W.make(name)
+            s1, sn, _ = oracle_times(cw, want_out=writes_out(name, cw))
+            cpu["workloads_ms"][name] = {"one_thread": round(1e3 * s1, 3),
+                                         "all_cores": round(1e3 * sn, 3)}
 
     if rank != 0:
         return 0

@@ -83,6 +83,8 @@ def test_cpu_baselines_time_the_oracle_on_every_token():
     wl = W.make("fused_norm_bs16")
     gbps, sec, passes = bench.oracle_gbps(wl, np.arange(wl.T))
     assert gbps > 0 and sec > 0 and passes >= 1
-    pg, psec, ppasses, threads = bench.oracle_gbps_parallel(wl)
-    assert pg > 0 and psec > 0 and ppasses >= 1
+    s1, sn, threads = bench.oracle_times(wl, want_out=True)
+    assert s1 > 0 and sn > 0
     assert threads == len(os.sched_getaffinity(0))
+    assert bench.writes_out("fused_norm_bs16", wl)
+    assert not bench.writes_out(bench.WORKLOAD, W.Workload(**{**wl.__dict__, "name": bench.WORKLOAD}))
