@@ -68,16 +68,27 @@ pack_kernel(const int32_t *__restrict__ expert_ids, const float *__restrict__ we
 }
 
 // Top-K gate, one warp per token.  Lane l holds logits l, l+32, l+64, ...
-// (EPL of them), each turned once into an order-preserving 32-bit key, and
-// keeps its two best unselected keys.  Each of the K rounds finds the
-// warp's largest unselected logit with two single-instruction warp
-// reductions: the maximum key, then the minimum expert id among the lanes
-// holding it (equal logits: lowest expert id first).  The winning lane
-// promotes its second-best key; only a lane that wins a second time before
-// it has rescanned goes over its keys again (at E = 256, K = 8 that is about
-// one rescan per token instead of K).  Lane k keeps round k's winner; the
-// weights are a softmax or a normalised sigmoid over the K kept logits
-// (recovered exactly from their keys), reduced across lanes 0..K-1.
+// (EPL of them), each turned once into an order-preserving 32-bit key.
+//
+// Usual case: a threshold, then a parallel ranking.  K rounds of a warp
+// maximum over the 32 lane maxima give theta, the K-th largest of them; the
+// K lanes above it hold K logits >= theta, so the token's top K all lie at
+// or above theta.  Those candidates (about K + 1 at E = 256, K = 8) are
+// compacted into shared memory, and lane i ranks candidate i against all of
+// them (larger logit first, equal logits lowest expert id first).
+//
+// When more than 32 logits reach theta (many equal logits), K rounds of
+// selection instead: each lane keeps its two best unselected keys, and each
+// round finds the warp's largest unselected logit with two single-
+// instruction warp reductions, the maximum key and then the minimum expert
+// id among the lanes holding it.  The winning lane promotes its second-best
+// key; only a lane that wins a second time before it has rescanned goes over
+// its keys again.
+//
+// Both leave the k-th selected logit on lane k; the weights are a softmax or
+// a normalised sigmoid over the K kept logits (recovered exactly from their
+// keys), reduced across lanes 0..K-1.  Both select the same logits in the
+// same order, so the outputs do not depend on which ran.
 constexpr int kRouteWarps = 4;
 
 // Order-preserving map from fp32 to uint32 (non-NaN inputs): a larger
@@ -118,6 +129,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kind,
                   int32_t *__restrict__ expert_ids, float *__restrict__ weights,
                   int32_t *__restrict__ packed) {
+    __shared__ uint32_t s_ck[kRouteWarps][32];   // candidate keys, then kept keys by rank
+    __shared__ uint32_t s_ci[kRouteWarps][32];   // their expert ids
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
@@ -130,28 +143,94 @@ topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kin
         key[j] = e < E ? order_key(__ldg(z + e)) : 0u;
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    uint32_t taken = 0u;                // slots this lane has given up
-    uint32_t b1, b2;
-    int j1, j2;
-    lane_best2(key, taken, &b1, &j1, &b2, &j2);
-    bool second_known = true;           // b2 is the lane's true second best
     uint32_t kept_key = 0u, top_key = 0u;
     int kept_id = 0;
-    for (int k = 0; k < K; ++k) {
-        const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, b1);
-        const uint32_t wi = __reduce_min_sync(
-            0xFFFFFFFFu, b1 == wk ? static_cast<uint32_t>(lane + 32 * j1) : 0xFFFFFFFFu);
-        if (lane == k) { kept_key = wk; kept_id = static_cast<int>(wi); }
-        if (k == 0) top_key = wk;
-        if (static_cast<int>(wi & 31u) == lane) {     // this lane's best was taken
-            taken |= 1u << j1;
-            if (second_known) {
-                b1 = b2;
-                j1 = j2;
-                second_known = false;
-            } else {
-                lane_best2(key, taken, &b1, &j1, &b2, &j2);
-                second_known = true;
+
+    // Threshold: the K-th largest of the 32 lane maxima.  The K lanes holding
+    // the largest maxima hold K logits at or above it, so every one of the
+    // token's top K is at or above it too.
+    uint32_t lane_max = 0u;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) lane_max = max(lane_max, key[j]);
+    uint32_t theta = 0u;
+    {
+        uint32_t mm = lane_max;
+        for (int k = 0; k < K; ++k) {
+            theta = __reduce_max_sync(0xFFFFFFFFu, mm);
+            const unsigned hold = __ballot_sync(0xFFFFFFFFu, mm == theta);
+            if (lane == __ffs(hold) - 1) mm = 0u;
+        }
+    }
+    // theta > 0 (E >= K logits sit on at least K lanes), so empty slots
+    // (key 0) never count as candidates.
+    uint32_t cmask = 0u;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) cmask |= (key[j] >= theta ? 1u : 0u) << j;
+    const unsigned cnt = __popc(cmask);
+    const unsigned C = __reduce_add_sync(0xFFFFFFFFu, cnt);
+    if (C <= 32u) {
+        const int w = threadIdx.x >> 5;
+        unsigned incl = cnt;            // inclusive prefix of the counts
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        unsigned pos = incl - cnt;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            if ((cmask >> j) & 1u) {
+                s_ck[w][pos] = key[j];
+                s_ci[w][pos] = static_cast<uint32_t>(lane + 32 * j);
+                ++pos;
+            }
+        }
+        __syncwarp();
+        // lane i ranks candidate i: larger logit first, then lower id
+        uint32_t ck = 0u, ci = 0u;
+        unsigned rank = 32u;
+        if (lane < static_cast<int>(C)) {
+            ck = s_ck[w][lane];
+            ci = s_ci[w][lane];
+            rank = 0u;
+            for (unsigned j = 0; j < C; ++j) {
+                const uint32_t kj = s_ck[w][j], ij = s_ci[w][j];
+                rank += (kj > ck || (kj == ck && ij < ci)) ? 1u : 0u;
+            }
+        }
+        __syncwarp();
+        if (rank < static_cast<unsigned>(K)) {
+            s_ck[w][rank] = ck;
+            s_ci[w][rank] = ci;
+        }
+        __syncwarp();
+        if (lane < K) {
+            kept_key = s_ck[w][lane];
+            kept_id = static_cast<int>(s_ci[w][lane]);
+        }
+        top_key = s_ck[w][0];
+    } else {                            // more than 32 candidates
+        uint32_t taken = 0u;            // slots this lane has given up
+        uint32_t b1, b2;
+        int j1, j2;
+        lane_best2(key, taken, &b1, &j1, &b2, &j2);
+        bool second_known = true;       // b2 is the lane's true second best
+        for (int k = 0; k < K; ++k) {
+            const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, b1);
+            const uint32_t wi = __reduce_min_sync(
+                0xFFFFFFFFu, b1 == wk ? static_cast<uint32_t>(lane + 32 * j1) : 0xFFFFFFFFu);
+            if (lane == k) { kept_key = wk; kept_id = static_cast<int>(wi); }
+            if (k == 0) top_key = wk;
+            if (static_cast<int>(wi & 31u) == lane) {   // this lane's best was taken
+                taken |= 1u << j1;
+                if (second_known) {
+                    b1 = b2;
+                    j1 = j2;
+                    second_known = false;
+                } else {
+                    lane_best2(key, taken, &b1, &j1, &b2, &j2);
+                    second_known = true;
+                }
             }
         }
     }

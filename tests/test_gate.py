@@ -116,3 +116,21 @@ def test_gate_then_finalize_with_packed_weights(cuda_lib, orc):
     torch.cuda.synchronize()
     ref = orc.moe_finalize(x, idx, packed, "packed", 2.5, shared)
     compare(out, ref, "gate->finalize: ")
+
+
+@pytest.mark.parametrize("n_top", [31, 32, 33, 40])
+def test_gate_candidate_count_boundary(cuda_lib, orc, n_top):
+    """n_top equal largest logits spread over the lanes: with 32 or fewer the
+    gate ranks the candidates at or above its threshold, with more it falls
+    back to round-by-round selection.  Either way the lowest ids win."""
+    rng = np.random.default_rng(n_top)
+    z = -np.abs(rng.standard_normal((9, 256))).astype(np.float32) - 1.0
+    z[:, :n_top] = 5.0
+    z[3, n_top + 7] = 6.0              # one token with a unique largest logit
+    for kind in ("softmax", "sigmoid"):
+        res = cuda_lib.topk_route(torch.from_numpy(z).cuda(), 8, kind, want_packed=True)
+        rid, rw = orc.topk_route(z, 8, kind)
+        ids = res["expert_ids"].cpu().numpy()
+        assert np.array_equal(ids, rid), (n_top, kind)
+        assert np.allclose(res["weights"].cpu().numpy(), rw, rtol=2e-6, atol=1e-9)
+        assert np.array_equal(ids[0], np.arange(8))
