@@ -71,11 +71,14 @@ pack_kernel(const int32_t *__restrict__ expert_ids, const float *__restrict__ we
 // (EPL of them), each turned once into an order-preserving 32-bit key.
 //
 // Usual case: a threshold, then a parallel ranking.  K rounds of a warp
-// maximum over the 32 lane maxima give theta, the K-th largest of them; the
-// K lanes above it hold K logits >= theta, so the token's top K all lie at
-// or above theta.  Those candidates (about K + 1 at E = 256, K = 8) are
-// compacted into shared memory, and lane i ranks candidate i against all of
-// them (larger logit first, equal logits lowest expert id first).
+// maximum over the 32 lane maxima give theta, the K-th largest of them (the
+// lane number rides in the low 5 bits, so each maximum names its lane; theta
+// keeps only the bits above them); the K lanes above it hold K logits >=
+// theta, so the token's top K all lie at or above theta.  Those candidates
+// (about K + 1 at E = 256, K = 8) are compacted into shared memory as one
+// (key, inverted id) word each, and lane i ranks candidate i against all of
+// them with one 64-bit comparison each (larger logit first, equal logits
+// lowest expert id first).
 //
 // When more than 32 logits reach theta (many equal logits), K rounds of
 // selection instead: each lane keeps its two best unselected keys, and each
@@ -129,8 +132,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kind,
                   int32_t *__restrict__ expert_ids, float *__restrict__ weights,
                   int32_t *__restrict__ packed) {
-    __shared__ uint32_t s_ck[kRouteWarps][32];   // candidate keys, then kept keys by rank
-    __shared__ uint32_t s_ci[kRouteWarps][32];   // their expert ids
+    __shared__ uint64_t s_cand[kRouteWarps][32];   // candidates, then the kept ones by rank
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
@@ -154,12 +156,14 @@ topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kin
     for (int j = 0; j < EPL; ++j) lane_max = max(lane_max, key[j]);
     uint32_t theta = 0u;
     {
-        uint32_t mm = lane_max;
+        // the lane number in the low 5 bits makes every lane's value unique,
+        // so one warp maximum names the winning lane
+        uint32_t mm = (lane_max & ~31u) | static_cast<uint32_t>(31 - lane);
         for (int k = 0; k < K; ++k) {
             theta = __reduce_max_sync(0xFFFFFFFFu, mm);
-            const unsigned hold = __ballot_sync(0xFFFFFFFFu, mm == theta);
-            if (lane == __ffs(hold) - 1) mm = 0u;
+            if (static_cast<int>(theta & 31u) == 31 - lane) mm = 0u;
         }
+        theta &= ~31u;   // K lanes have maxima >= theta: still a lower bound
     }
     // theta > 0 (E >= K logits sit on at least K lanes), so empty slots
     // (key 0) never count as candidates.
@@ -177,38 +181,35 @@ topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kin
             if (lane >= o) incl += v;
         }
         unsigned pos = incl - cnt;
+        // (key, inverted id) in one word: a larger word is a larger logit,
+        // or an equal logit with a lower id
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
             if ((cmask >> j) & 1u) {
-                s_ck[w][pos] = key[j];
-                s_ci[w][pos] = static_cast<uint32_t>(lane + 32 * j);
+                s_cand[w][pos] = (static_cast<uint64_t>(key[j]) << 32) |
+                                 (0xFFFFFFFFu - static_cast<uint32_t>(lane + 32 * j));
                 ++pos;
             }
         }
         __syncwarp();
-        // lane i ranks candidate i: larger logit first, then lower id
-        uint32_t ck = 0u, ci = 0u;
+        // lane i ranks candidate i against all of them
+        uint64_t mine = 0u;
         unsigned rank = 32u;
         if (lane < static_cast<int>(C)) {
-            ck = s_ck[w][lane];
-            ci = s_ci[w][lane];
+            mine = s_cand[w][lane];
             rank = 0u;
-            for (unsigned j = 0; j < C; ++j) {
-                const uint32_t kj = s_ck[w][j], ij = s_ci[w][j];
-                rank += (kj > ck || (kj == ck && ij < ci)) ? 1u : 0u;
-            }
+#pragma unroll 4
+            for (unsigned j = 0; j < C; ++j) rank += s_cand[w][j] > mine ? 1u : 0u;
         }
         __syncwarp();
-        if (rank < static_cast<unsigned>(K)) {
-            s_ck[w][rank] = ck;
-            s_ci[w][rank] = ci;
-        }
+        if (rank < static_cast<unsigned>(K)) s_cand[w][rank] = mine;
         __syncwarp();
         if (lane < K) {
-            kept_key = s_ck[w][lane];
-            kept_id = static_cast<int>(s_ci[w][lane]);
+            const uint64_t kept = s_cand[w][lane];
+            kept_key = static_cast<uint32_t>(kept >> 32);
+            kept_id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kept));
         }
-        top_key = s_ck[w][0];
+        top_key = static_cast<uint32_t>(s_cand[w][0] >> 32);
     } else {                            // more than 32 candidates
         uint32_t taken = 0u;            // slots this lane has given up
         uint32_t b1, b2;
