@@ -75,6 +75,63 @@ def pin_golden_hand_worked(orc):
         assert np.array_equal(r2["out"], np.array(g["out"], np.float64)), kind
 
 
+def _exact_weight(wkind, word):
+    """A routing weight as an exact rational, decoded here independently of
+    the oracle: fp32 value, bf16 bits, or the low half of a packed word."""
+    if wkind == "fp32":
+        return Fraction(float(np.float32(word)))
+    bits = int(word) & 0xFFFF
+    return Fraction(float(np.array([bits << 16], np.uint32).view(np.float32)[0]))
+
+
+def pin_exact_rational_brute_force(orc):
+    """Brute force in exact rational arithmetic on tiny problems.  Every
+    input is a binary fraction, so out and residual_out have exact values;
+    the oracle's double results must lie within a few ulps of them.
+    norm_out uses a 50-digit square root."""
+    import decimal
+    decimal.getcontext().prec = 50
+    problems = []
+    wl = synth("exact_tiny", T=4, K=2, H=64, E=8, tile=4, P=32, weight_rule="softmax",
+               routed_scale=1.0, seed=0)
+    problems.append((wl.permuted_out, wl.idx, wl.weights, wl.wkind, 1.0, wl.shared, None, None))
+    for seed, wkind in ((1, "fp32"), (2, "bf16"), (3, "packed")):
+        x, idx, w, shared, res, gamma = _rand_problem(40 + seed, T=3, K=4, H=24, with_norm=True)
+        w[:, 1] = -w[:, 1]            # a negative weight in every token
+        if wkind == "bf16":
+            w = _bits(w)
+        elif wkind == "packed":    # words built here, with torch's bf16 rounding
+            experts = (7 * np.arange(4)[None, :] + np.arange(3)[:, None]).astype(np.uint32)
+            w = ((experts << 16) | _bits(w).astype(np.uint32)).view(np.int32)
+        problems.append((x, idx, w, wkind, 2.5, shared, res, gamma))
+    eps = 1e-6
+    for x, idx, w, wkind, scale, shared, res, gamma in problems:
+        got = orc.moe_finalize(x, idx, w, wkind, scale, shared, res, gamma, eps)
+        xf = bf16_bits_to_f32(x).astype(np.float64)
+        T, K = idx.shape
+        H = x.shape[1]
+        for t in range(T):
+            wk = [_exact_weight(wkind, w[t, k]) * Fraction(scale) for k in range(K)]
+            m = [sum(wk[k] * Fraction(float(xf[idx[t, k], h])) for k in range(K)) +
+                 Fraction(float(bf16_bits_to_f32(shared[t, h]))) for h in range(H)]
+            for h in range(H):
+                assert abs(Fraction(got["out"][t, h]) - m[h]) <= \
+                    Fraction(2.0 ** -50) * (abs(m[h]) + 1), ("out", t, h)
+            if res is None:
+                continue
+            s = [m[h] + Fraction(float(bf16_bits_to_f32(res[t, h]))) for h in range(H)]
+            for h in range(H):
+                assert abs(Fraction(got["residual_out"][t, h]) - s[h]) <= \
+                    Fraction(2.0 ** -50) * (abs(s[h]) + 1), ("residual_out", t, h)
+            ms = sum(v * v for v in s) / H + Fraction(eps)
+            inv = 1 / (decimal.Decimal(ms.numerator) / decimal.Decimal(ms.denominator)).sqrt()
+            for h in range(H):
+                want = float(decimal.Decimal(s[h].numerator) / decimal.Decimal(s[h].denominator)
+                             * inv * decimal.Decimal(float(bf16_bits_to_f32(gamma[h]))))
+                assert math.isclose(got["norm_out"][t, h], want, rel_tol=1e-12, abs_tol=1e-14), \
+                    ("norm_out", t, h)
+
+
 def pin_k1_identity(orc):
     """K=1, weight 1, scale 1, zero shared: out is the gathered row, exactly."""
     x, idx, _, shared, _, _ = _rand_problem(1, T=7, K=1, H=33)
