@@ -61,3 +61,19 @@ def test_only_the_permitted_entry_points_load_the_oracle():
         allowed = {"bench.py": {"oracle_gbps", "oracle_times"},
                    "__graft_entry__.py": {"build", "smoke"}}[name]
         assert users and users <= allowed, (name, users)
+
+
+def test_no_triton_no_compile_no_cpu_compute_in_the_product():
+    """The product (package, kernels, bench, entry points) uses no Triton
+    and no torch.compile, and the binding has no compute of its own: it only
+    checks, allocates and calls the library."""
+    product = list(_files(PKG, (".py", ".cu", ".cuh", ".c"))) + \
+        [os.path.join(ROOT, n) for n in ("bench.py", "__graft_entry__.py")]
+    for path in product:
+        text = open(path).read()
+        assert not re.search(r"^\s*(import|from)\s+triton", text, re.M), path
+        assert "torch.compile" not in text, path
+    binding = open(os.path.join(PKG, "_abi.py")).read()
+    for op in ("torch.matmul", "torch.einsum", "index_select", "torch.rsqrt", "rms_norm",
+               ".sum(", ".mean(", "torch.topk", "torch.sigmoid", "torch.softmax"):
+        assert op not in binding, op
