@@ -493,9 +493,10 @@ def oracle_gbps(wl, tokens, repeat_until_s=0.0):
     return nbytes * passes / el / 1e9, el / passes, passes
 
 
-def oracle_times(wl, want_out, reps=3):
+def oracle_times(wl, want_out, reps=3, min_seconds=0.0):
     """Median seconds of one oracle pass over every token of ``wl``: on one
-    thread, and as token blocks from one thread per host core.
+    thread (at least ``reps`` passes, more until ``min_seconds`` have run),
+    and as token blocks from one thread per host core (``reps`` passes).
 
     The oracle is unchanged: each thread calls it on a contiguous block of
     tokens (ctypes releases the GIL for the duration of the C call).  Returns
@@ -511,7 +512,7 @@ def oracle_times(wl, want_out, reps=3):
                          wl.gamma, wl.eps, want_out=want_out)
 
     single = []
-    for _ in range(reps):
+    while len(single) < reps or sum(single) < min_seconds:
         t0 = time.perf_counter()
         run(0, wl.T)
         single.append(time.perf_counter() - t0)
@@ -627,11 +628,11 @@ def run_ours(args, ws, rank, local):
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
-        sec, psec, nthr = oracle_times(wl, want_out=False)
+        sec, psec, nthr = oracle_times(wl, want_out=False, min_seconds=10.0)
         cpu = {"value": round(nbytes / sec / 1e9, 4), "unit": "GB/s", "cores": 1,
                "kind": "oracle",
-               "sample": f"all {wl.T} tokens of {WORKLOAD}, median of 3 passes, "
-                         f"{sec:.2f} s per pass, single-threaded fp64"}
+               "sample": f"all {wl.T} tokens of {WORKLOAD}, repeated for at least 10 s, "
+                         f"median {sec:.2f} s per pass, single-threaded fp64"}
         cpu["all_cores"] = {"value": round(nbytes / psec / 1e9, 4), "unit": "GB/s",
                             "cores": nthr,
                             "sample": f"all {wl.T} tokens, median of 3 passes, {psec:.3f} s "
