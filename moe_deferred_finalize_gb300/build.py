@@ -76,9 +76,10 @@ FASTCALL_SRC = os.path.join(CSRC, "fastcall.c")
 
 
 def build_fastcall() -> str:
-    """Compile the _fastcall CPython extension (bound-call replay, no CUDA
-    code) next to the library; returns its path, or "" when the Python
-    headers are not available (the binding then uses ctypes for every call)."""
+    """Compile the _fastcall CPython extension (direct and bound calls of
+    moe_finalize_ex; no CUDA code) next to the library; returns its path, or
+    "" when the Python headers are not available (the binding then uses
+    ctypes for every call)."""
     import sysconfig
     inc = sysconfig.get_paths()["include"]
     out = os.path.join(PKG, "_fastcall" + sysconfig.get_config_var("EXT_SUFFIX"))
