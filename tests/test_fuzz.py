@@ -11,7 +11,7 @@ from gpu_util import bf16_dev, compare, run_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 40
+N_CASES = 80
 
 
 def _case(i):
