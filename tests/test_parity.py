@@ -6,6 +6,7 @@ zero weights, identical tokens, launch shape changes for out/residual_out).
 """
 import ctypes
 import dataclasses
+import types
 
 import numpy as np
 import pytest
@@ -15,6 +16,7 @@ from moe_deferred_finalize_gb300 import workloads as W
 
 from gpu_util import (assert_close, bf16_dev, bits_of, compare, f64_of, run_gpu, run_oracle,
                       to_device)
+from test_unfused import _check as check_unfused
 
 pytestmark = pytest.mark.gpu
 
@@ -270,6 +272,15 @@ def test_token_offsets_beyond_2_to_the_31_elements(cuda_lib, orc):
                                rs_s if norm else None, gamma if norm else None, 1e-6)
         compare({k: v.index_select(0, sel) for k, v in res.items() if v is not None}, ref,
                 f"tokens past 2^31 elements, norm={norm}: ")
+        # the unfused A/B kernels index the same tensors (their own tolerance:
+        # they also round the combined rows to bf16)
+        unf = cuda_lib.moe_finalize_unfused(x, idx_d, w_d, "fp32", shared, routed_scale=2.5,
+                                            eps=1e-6, **kw)
+        torch.cuda.synchronize()
+        sampled = types.SimpleNamespace(shared=sh_s, with_norm=norm, eps=1e-6, gamma=gamma)
+        check_unfused({k: v.index_select(0, sel) for k, v in unf.items() if v is not None},
+                      ref, sampled, f"unfused, tokens past 2^31 elements, norm={norm}: ")
+        del unf
         # the other rows: routed sum only (zero shared / residual), in bf16
         routed = (w_d[:, :1] * 2.5 * x.float()[idx_d[:, 0]] +
                   w_d[:, 1:] * 2.5 * x.float()[idx_d[:, 1]])
