@@ -350,6 +350,13 @@ moef_status moe_finalize_check_indices(const int32_t *idx_map, int T, int K,
 /* Static English text for a status value (never NULL). */
 const char *moef_status_string(moef_status s);
 
+/* Version of this interface: raised whenever an entry point's arguments,
+ * their meaning or a struct layout changes.  moef_abi_version() returns the
+ * value the library was built with; a caller compiled against this header
+ * should refuse a library that reports another. */
+#define MOEF_ABI_VERSION 1
+int moef_abi_version(void);
+
 #ifdef __cplusplus
 }
 #endif

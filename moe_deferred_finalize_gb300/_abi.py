@@ -15,6 +15,7 @@ from typing import Optional
 import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_finalize.so")
+ABI_VERSION = 1     # MOEF_ABI_VERSION of include/moe_finalize.h
 
 WKIND = {"fp32": 0, "bf16": 1, "packed": 2}
 _WDTYPE = {"fp32": (torch.float32,), "bf16": (torch.bfloat16, torch.int16),
@@ -78,6 +79,12 @@ def _lib():
         lib.moe_finalize_check_indices.restype = i32
         lib.moef_status_string.argtypes = [i32]
         lib.moef_status_string.restype = ctypes.c_char_p
+        lib.moef_abi_version.argtypes = []
+        lib.moef_abi_version.restype = i32
+        if lib.moef_abi_version() != ABI_VERSION:
+            raise RuntimeError(
+                f"libmoe_finalize.so reports interface version {lib.moef_abi_version()}, "
+                f"this binding expects {ABI_VERSION}: rebuild the library")
         _LIB = lib
     return _LIB
 

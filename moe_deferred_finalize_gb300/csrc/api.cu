@@ -66,6 +66,8 @@ moef_status cuda_status(cudaError_t err) {
 
 extern "C" {
 
+int moef_abi_version(void) { return MOEF_ABI_VERSION; }
+
 const char *moef_status_string(moef_status s) {
     switch (s) {
         case MOEF_OK: return "ok";

@@ -42,6 +42,21 @@ def test_library_exports_every_declared_symbol(mf):
         assert hasattr(lib, name), name
 
 
+def test_abi_version_matches_header_and_binding(mf):
+    text = open(os.path.join(HEADER_DIR, "moe_finalize.h")).read()
+    version = int(re.search(r"#define MOEF_ABI_VERSION (\d+)", text).group(1))
+    from moe_deferred_finalize_gb300 import _abi
+    assert mf.lib().moef_abi_version() == version == _abi.ABI_VERSION
+
+
+def test_library_of_another_interface_version_is_refused(mf, monkeypatch):
+    from moe_deferred_finalize_gb300 import _abi
+    monkeypatch.setattr(_abi, "_LIB", None)
+    monkeypatch.setattr(_abi, "ABI_VERSION", _abi.ABI_VERSION + 1)
+    with pytest.raises(RuntimeError, match="interface version"):
+        _abi._lib()
+
+
 def test_unknown_flags_rejected(mf):
     f = mf.lib().moe_finalize_ex
     assert f(A, 16, A, A, 0, 1.0, A, None, None, 1e-6, A, None, None, 0, 2, 8, 0, 0, 2, None) == 4
