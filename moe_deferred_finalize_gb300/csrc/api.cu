@@ -95,8 +95,10 @@ const char *moef_status_string(moef_status s) {
 //    CTA, 4-CTA clusters at H = 7168), and the split is halved while the
 //    grid exceeds about 3.5 CTAs per SM (the best grids measured held
 //    384-512 CTAs); with no split one CTA takes a whole row (256 threads
-//    below 4 rows per SM, then 128).  7-CTA clusters at T = 512 were 1.5x
-//    slower than this.
+//    below 4 rows per SM or for rows of at most 512 vectors, then 128).
+//    7-CTA clusters at T = 512 were 1.5x slower than this.  At H = 2048 and
+//    4096, T = 2048, 256 threads beat 128 by 5.8 % and 2.9 %; at H = 5120
+//    and 7168, 128 threads win.
 // A row with RMSNorm must fit one pass of one CTA (256 x 8 vectors) or one
 // cluster of at most 16 such CTAs.
 moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, int num_sms,
@@ -121,7 +123,13 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, in
         while (splits > row_fit && splits > 1 && rows * splits > cap) splits = ceil_div(splits, 2);
         if (splits < row_fit) splits = row_fit;
         if (splits > kMaxCluster) splits = kMaxCluster;
-        if (splits == 1) threads_auto = rows < 4 * static_cast<int64_t>(num_sms) ? kMaxThreads : 128;
+        // one CTA per row: 256 threads below 4 rows per SM, and for rows of at
+        // most 512 vectors (one or two per thread, all row loads in flight at
+        // once); otherwise 128 threads with up to 8 vectors each
+        if (splits == 1)
+            threads_auto = (rows < 4 * static_cast<int64_t>(num_sms) || nvec <= 2 * kMaxThreads)
+                               ? kMaxThreads
+                               : 128;
     } else {
         // 128-vector slices; if that grid would need between one and two
         // waves of 128-thread CTAs (8 per SM at 64 registers), 64-thread CTAs
