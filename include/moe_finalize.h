@@ -137,9 +137,10 @@ typedef enum {
  * The call allocates nothing and does not synchronise, so it may be
  * captured in a CUDA graph ("[Kimi K2.5] Fuse deferred MoE finalize ...",
  * Key modifications: workspace sized before capture, never grown inside
- * captured graphs).  Its first call on a device with a given RMSNorm split
- * wider than 8 CTAs sets a kernel attribute; make that first call before
- * any capture.
+ * captured graphs).  The first call on a device that splits an RMSNorm row
+ * over more than 8 CTAs sets a kernel attribute (once per kernel build: K
+ * fixed at 8 on grids above one CTA per SM, or any K); make such calls, with
+ * the shapes that will be captured, before any capture.
  */
 moef_status moe_finalize(const void *permuted_out, int64_t P,
                          const int32_t *idx_map,
