@@ -53,8 +53,9 @@ CASES = [
     (300, 8, 7168, "packed", False),
     (300, 6, 1000, "fp32", True),
     (700, 8, 7168, "fp32", True),      # just past the latency regime
-    (2, 4, 16384, "fp32", True),       # cluster of 16 CTAs
-    (40, 2, 24576, "fp32", True),      # bandwidth regime, norm row over 2 CTAs
+    (2, 4, 16384, "fp32", True),       # cluster of 8 CTAs
+    (2, 4, 32768, "bf16", True),       # cluster of 16 CTAs (non-portable size)
+    (40, 2, 24576, "fp32", True),      # norm rows over 12-CTA clusters
     (33, 5, 40000, "bf16", False),     # several passes per slice without norm
     (9, 4, 4098, "fp32", True),        # H % 8 == 2: scalar path with cluster
     (2048, 8, 4096, "fp32", True),     # bandwidth regime, other hidden sizes
@@ -373,8 +374,17 @@ def test_fp32_weights_read_as_bf16_fail_parity(cuda_lib, orc):
         assert_close(f64_of(out), run_oracle(orc, wl)["out"], "misread weights")
 
 
-def test_graph_capture_replay(cuda_lib, orc):
-    wl = W.make("fused_norm_bs16")
+def _wide_cluster_workload():
+    """T=2, H=32768 with RMSNorm: rows split over a 16-CTA cluster."""
+    return W.synth("wide", T=2, K=4, H=32768, E=64, tile=8, P=64, weight_rule="sigmoid",
+                   routed_scale=1.0, with_norm=True, seed=21, require_all=False)
+
+
+@pytest.mark.parametrize("which", ["fused_norm_bs16", "cluster16"])
+def test_graph_capture_replay(cuda_lib, orc, which):
+    wl = W.make(which) if which != "cluster16" else _wide_cluster_workload()
+    if which == "cluster16":
+        assert cuda_lib.plan(wl.T, wl.K, wl.H, True)["cluster"] == 16
     dev = to_device(wl)
     outs = {k: torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
             for k in ("out", "residual_out", "norm_out")}
@@ -384,7 +394,7 @@ def test_graph_capture_replay(cuda_lib, orc):
                               routed_scale=1.0, residual=dev["residual"], gamma=dev["gamma"],
                               eps=wl.eps, **outs)
 
-    step()                      # first call outside capture
+    step()                      # first call outside capture (sets any cluster attribute)
     torch.cuda.synchronize()
     for t in outs.values():
         t.zero_()

@@ -23,7 +23,7 @@ def _workloads():
         W.make("decode_bs1_packed"),                       # any-K build, 7 CTAs
         W.make("decode_bs256"),                            # K=8 build, 1792 CTAs
         W.make("fused_norm_bs16"),                         # 4-CTA clusters
-        W.synth("c16", T=2, K=4, H=16384, E=64, tile=8, P=64, weight_rule="sigmoid",
+        W.synth("c16", T=2, K=4, H=32768, E=64, tile=8, P=64, weight_rule="sigmoid",
                 routed_scale=2.5, with_norm=True, seed=5, require_all=False),  # 16-CTA clusters
     ]
 
