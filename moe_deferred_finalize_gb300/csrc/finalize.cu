@@ -301,6 +301,11 @@ cudaError_t launch_vec(const FinalizeParams &p, const moef_plan &plan, int num_s
 
 cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan, int num_sms,
                             cudaStream_t stream) {
+    // The RMSNorm form makes one pass over its slice (the sum of squares of
+    // the whole row must be complete before the second pass), so its plan
+    // must give every vector of the slice a thread in that pass.
+    if (p.residual && static_cast<int64_t>(plan.threads) * plan.vpt < plan.slice)
+        return cudaErrorInvalidValue;
     if (plan.vec == 8) return launch_vec<8>(p, plan, num_sms, stream);
     if (plan.vec == 1) return launch_vec<1>(p, plan, num_sms, stream);
     return cudaErrorInvalidValue;

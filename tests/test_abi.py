@@ -205,6 +205,28 @@ def test_plan_invariants(mf):
                         assert p["cluster"] == 1
 
 
+def test_every_accepted_norm_plan_covers_its_slice_in_one_pass(mf):
+    """The RMSNorm kernel makes one pass over its slice, and its launcher
+    refuses a plan that leaves vectors without a thread; so every plan the
+    planner accepts with RMSNorm, automatic or hinted, must cover its slice."""
+    accepted = 0
+    for H in (8, 40, 64, 1000, 2048, 4096, 4104, 5120, 7168, 8192, 16384, 32768, 65536,
+              262144):
+        for T in (1, 16, 192, 640, 4096):
+            for splits in (0, 1, 2, 3, 4, 7, 8, 12, 16):
+                for threads in (0, 32, 64, 128, 256):
+                    for vec_ok in (True, False):
+                        try:
+                            p = mf.plan(T, 8, H, True, vec_ok, splits=splits, threads=threads)
+                        except mf.MoefError as e:
+                            assert e.status in (2, 4)
+                            continue
+                        accepted += 1
+                        assert p["threads"] * p["vpt"] >= p["slice"], (H, T, splits, threads, p)
+                        assert p["splits"] * p["slice"] >= H // p["vec"]
+    assert accepted > 1000
+
+
 def test_plan_size_limits(mf):
     # the grid is T * splits CTAs and must fit a signed 32-bit count
     p = mf.plan(2**31 // 8, 8, 7168, False)
