@@ -46,6 +46,10 @@ class Oracle:
         lib.oref_rmsnorm_bf16.argtypes = [p, p, ctypes.c_double, i64, i64, p]
         lib.oref_pack_topk_ids.restype = None
         lib.oref_pack_topk_ids.argtypes = [p, p, i64, p]
+        lib.oref_moe_finalize_ar.restype = ctypes.c_int
+        lib.oref_moe_finalize_ar.argtypes = [i64, p, p, i64, p, p, ctypes.c_int,
+                                             ctypes.c_double, p, p, p, ctypes.c_double,
+                                             i64, i64, p, p, p]
         lib.oref_topk_route.restype = ctypes.c_int
         lib.oref_topk_route.argtypes = [p, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p]
         self.lib = lib
@@ -86,6 +90,58 @@ class Oracle:
             T, K, _ptr(out), _ptr(res_out), _ptr(norm_out))
         if rc == -1:
             raise ValueError("index outside [0, P)")
+        if rc != 0:
+            raise ValueError(f"oracle returned {rc}")
+        res = {"out": out}
+        if residual is not None:
+            res["residual_out"] = res_out
+            res["norm_out"] = norm_out
+        return res
+
+    def moe_finalize_ar(self, ranks, wkind, routed_scale, residual=None, gamma=None,
+                        eps=1e-6, want_out=True):
+        """fp64 deferred finalize of R tensor-parallel ranks, all-reduced,
+        then residual + RMSNorm.
+
+        ranks: a list of R dicts with "permuted_out" uint16 [P_r, H],
+        "idx" int32 [T, K], "weights" [T, K] (encoding ``wkind``, the same
+        for every rank) and "shared" uint16 [T, H].  residual uint16 [T, H]
+        and gamma uint16 [H] are common to all ranks.  Returns a dict like
+        ``moe_finalize``.  Raises ValueError on an index outside a rank's
+        [0, P_r).
+        """
+        if not ranks:
+            raise ValueError("at least one rank")
+        R = len(ranks)
+        xs = [_c(r["permuted_out"], np.uint16) for r in ranks]
+        idxs = [_c(r["idx"], np.int32) for r in ranks]
+        ws = [_c(r["weights"], _WDTYPE[wkind]) for r in ranks]
+        shs = [_c(r["shared"], np.uint16) for r in ranks]
+        H = xs[0].shape[1]
+        T, K = idxs[0].shape
+        for x, i, w, sh in zip(xs, idxs, ws, shs):
+            if x.ndim != 2 or x.shape[1] != H or i.shape != (T, K) or w.shape != (T, K) \
+                    or sh.shape != (T, H):
+                raise ValueError("shape mismatch between ranks")
+        if (residual is None) != (gamma is None):
+            raise ValueError("residual and gamma go together")
+        residual = _c(residual, np.uint16)
+        gamma = _c(gamma, np.uint16)
+        out = np.empty((T, H), np.float64) if want_out else None
+        res_out = norm_out = None
+        if residual is not None:
+            if residual.shape != (T, H) or gamma.shape != (H,):
+                raise ValueError("shape mismatch")
+            res_out = np.empty((T, H), np.float64)
+            norm_out = np.empty((T, H), np.float64)
+        ptrs = lambda arrs: (ctypes.c_void_p * R)(*[a.ctypes.data for a in arrs])
+        P = (ctypes.c_int64 * R)(*[x.shape[0] for x in xs])
+        rc = self.lib.oref_moe_finalize_ar(
+            R, ptrs(xs), P, H, ptrs(idxs), ptrs(ws), _WKIND[wkind], float(routed_scale),
+            ptrs(shs), _ptr(residual), _ptr(gamma), float(eps), T, K,
+            _ptr(out), _ptr(res_out), _ptr(norm_out))
+        if rc == -1:
+            raise ValueError("index outside [0, P) on some rank")
         if rc != 0:
             raise ValueError(f"oracle returned {rc}")
         res = {"out": out}
@@ -158,6 +214,10 @@ def default() -> Oracle:
 
 def moe_finalize(*args, **kwargs):
     return default().moe_finalize(*args, **kwargs)
+
+
+def moe_finalize_ar(*args, **kwargs):
+    return default().moe_finalize_ar(*args, **kwargs)
 
 
 def rmsnorm_bf16(*args, **kwargs):

@@ -52,6 +52,10 @@
  * zero scale, slot-permutation invariance, linearity, NaN-filled padding,
  * RMSNorm closed forms and a library RMSNorm, hand-worked golden values,
  * exhaustive pack/unpack round trips against a library bf16 conversion.
+ * For the all-reduce-fused form (oref_moe_finalize_ar, at the end): a
+ * hand-worked two-rank golden case, one rank = the plain finalize, R ranks =
+ * one rank over all the ranks' slots with the shared outputs summed, rank
+ * order, an exact tensor-parallel split, per-rank index bounds.
  */
 #include <math.h>
 #include <stdint.h>
@@ -205,6 +209,70 @@ int oref_moe_finalize(const uint16_t *permuted_out, int64_t P, int64_t H,
                 m += w * bf16_to_double(row[h]);
             }
             m += bf16_to_double(shared[t * H + h]);
+            if (out) out[t * H + h] = m;
+            if (residual) residual_out[t * H + h] = m + bf16_to_double(residual[t * H + h]);
+        }
+    }
+    if (residual) rmsnorm_rows_double(residual_out, gamma, eps, T, H, norm_out);
+    return 0;
+}
+
+/* The deferred finalize fused with the tensor-parallel all-reduce, residual
+ * add and RMSNorm ("[Kimi K2.5] Fuse deferred MoE finalize into next-layer
+ * AR + residual + RMSNorm", Summary: weighted expert combine + shared-expert
+ * add + all-reduce + residual + RMSNorm in one kernel, residual_out kept;
+ * Numerics & speed: the all-reduce runs over the finalized token rows, and
+ * the separate-finalize fallback computes the same thing as a finalize
+ * followed by an all-reduce fused with residual + RMSNorm).
+ *
+ * R ranks of one tensor-parallel group each hold their own expert output
+ * rows, row map, routing weights and shared-expert output (each a partial
+ * sum over that rank's slice of the expert and shared-expert weights).  For
+ * token t and column h:
+ *
+ *   p_r[t,h] = sum_k (routed_scale * w_r[t,k]) * x_r[idx_r[t,k], h]
+ *              + shared_r[t,h]                   (rank r's own finalize)
+ *   m[t,h]   = sum_r p_r[t,h]                    (the all-reduce)
+ *   out      = m
+ *   if a residual is given:
+ *     s            = m + residual[t,h]
+ *     residual_out = s
+ *     norm_out     = s / sqrt(mean_h(s^2) + eps) * gamma[h]
+ *
+ * The residual and gamma are the same on every rank, so they appear once;
+ * every rank obtains the same outputs.  All arithmetic in double from the
+ * exact input values, ranks summed r = 0..R-1.
+ *
+ * permuted_out[r], P[r], idx[r], weights[r], shared[r]: rank r's operands,
+ * shaped as for oref_moe_finalize (weights in one encoding, wkind, for all
+ * ranks).  Returns 0; -1 when an index of some rank lies outside [0, P[r]);
+ * -2 for an unknown wkind; -3 for R < 1. */
+int oref_moe_finalize_ar(int64_t R, const uint16_t *const *permuted_out, const int64_t *P,
+                         int64_t H, const int32_t *const *idx, const void *const *weights,
+                         int wkind, double routed_scale, const uint16_t *const *shared,
+                         const uint16_t *residual, const uint16_t *gamma, double eps,
+                         int64_t T, int64_t K,
+                         double *out, double *residual_out, double *norm_out) {
+    if (R < 1) return -3;
+    if (wkind != OREF_W_FP32 && wkind != OREF_W_BF16 && wkind != OREF_W_PACKED)
+        return -2;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t i = 0; i < T * K; ++i)
+            if (idx[r][i] < 0 || (int64_t)idx[r][i] >= P[r]) return -1;
+
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            double m = 0.0;
+            for (int64_t r = 0; r < R; ++r) {
+                double partial = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    double w = routed_scale * decode_weight(weights[r], wkind, t * K + k);
+                    const uint16_t *row = permuted_out[r] + (int64_t)idx[r][t * K + k] * H;
+                    partial += w * bf16_to_double(row[h]);
+                }
+                partial += bf16_to_double(shared[r][t * H + h]);
+                m += partial;
+            }
             if (out) out[t * H + h] = m;
             if (residual) residual_out[t * H + h] = m + bf16_to_double(residual[t * H + h]);
         }

@@ -434,4 +434,135 @@ def pin_weight_decode_exhaustive(orc):
     assert np.array_equal(r["out"], want)
 
 
+# ------------------------------------------- all-reduce-fused finalize pins
+#
+# The finalize of R tensor-parallel ranks summed over the ranks, then the
+# residual add and RMSNorm ("[Kimi K2.5] Fuse deferred MoE finalize into
+# next-layer AR + residual + RMSNorm", Summary; Numerics & speed).
+
+
+def _rand_ranks(seed, R, T=4, K=3, H=24, wkind="fp32", P=None):
+    """R ranks with their own rows (different row counts), maps, weights and
+    shared outputs."""
+    ranks = []
+    for r in range(R):
+        x, idx, w, shared, _, _ = _rand_problem(seed * 100 + r, T=T, K=K, H=H,
+                                                P=(P or T * K + 5) + 3 * r)
+        w[:, 0] = -w[:, 0]                 # a negative weight on every rank
+        if wkind == "bf16":
+            w = _bits(w)
+        elif wkind == "packed":
+            experts = (5 * np.arange(K)[None, :] + np.arange(T)[:, None] + r).astype(np.uint32)
+            w = ((experts << 16) | _bits(w).astype(np.uint32)).view(np.int32)
+        ranks.append({"permuted_out": x, "idx": idx, "weights": w, "shared": shared})
+    return ranks
+
+
+def _torch_rms_norm(s, gamma_bits, eps):
+    """RMSNorm of float64 rows by torch's own routine."""
+    g = torch.from_numpy(bf16_bits_to_f32(gamma_bits).astype(np.float64))
+    return torch.nn.functional.rms_norm(torch.from_numpy(s), (s.shape[1],), weight=g,
+                                        eps=eps).numpy()
+
+
+def pin_ar_golden_hand_worked(orc):
+    g = _load("hand_worked_ar_r2_t2_k2_h3.json")
+    ranks = [{"permuted_out": _bits(r["permuted_out"]), "idx": np.array(r["idx"], np.int32),
+              "weights": np.array(r["weights_fp32"], np.float32), "shared": _bits(r["shared"])}
+             for r in g["ranks"]]
+    res, gamma = _bits(g["residual"]), _bits(g["gamma"])
+    got = orc.moe_finalize_ar(ranks, "fp32", g["routed_scale"], res, gamma, g["eps"])
+    assert np.array_equal(got["out"], np.array(g["out"], np.float64)), got["out"]
+    assert np.array_equal(got["residual_out"], np.array(g["residual_out"], np.float64))
+    want_norm = np.array([[float(Fraction(v)) for v in row] for row in g["norm_out"]])
+    assert np.allclose(got["norm_out"], want_norm, rtol=1e-15, atol=0), got["norm_out"]
+    # each rank's own partial is the single-rank finalize of its operands
+    for rk, r in zip(ranks, g["ranks"]):
+        one = orc.moe_finalize(rk["permuted_out"], rk["idx"], rk["weights"], "fp32",
+                               g["routed_scale"], rk["shared"])
+        assert np.array_equal(one["out"], np.array(r["partial"], np.float64))
+
+
+def pin_ar_single_rank_is_the_finalize(orc):
+    """With one rank the all-reduce is the identity: exactly the finalize."""
+    for seed, wkind in ((1, "fp32"), (2, "bf16"), (3, "packed")):
+        rk = _rand_ranks(seed, 1, wkind=wkind)[0]
+        _, _, _, _, res, gamma = _rand_problem(seed, T=4, K=3, H=24, with_norm=True)
+        a = orc.moe_finalize_ar([rk], wkind, 2.5, res, gamma, 1e-6)
+        b = orc.moe_finalize(rk["permuted_out"], rk["idx"], rk["weights"], wkind, 2.5,
+                             rk["shared"], res, gamma, 1e-6)
+        for key in b:
+            assert np.array_equal(a[key], b[key]), (wkind, key)
+
+
+def pin_ar_equals_one_rank_over_all_slots(orc):
+    """R ranks equal one rank whose buffer stacks the ranks' rows and whose
+    K*R slots are the ranks' slots side by side (rows offset into the stack),
+    plus every rank's shared output, summed here in double; the RMSNorm of
+    that sum by torch's routine."""
+    for seed, R, wkind in ((11, 2, "fp32"), (12, 3, "bf16"), (13, 4, "packed"),
+                           (14, 8, "fp32")):
+        ranks = _rand_ranks(seed, R, wkind=wkind)
+        _, _, _, _, res, gamma = _rand_problem(seed, T=4, K=3, H=24, with_norm=True)
+        eps = 1e-6
+        got = orc.moe_finalize_ar(ranks, wkind, 2.5, res, gamma, eps)
+        offsets = np.cumsum([0] + [rk["permuted_out"].shape[0] for rk in ranks])[:-1]
+        x = np.concatenate([rk["permuted_out"] for rk in ranks])
+        idx = np.concatenate([rk["idx"] + off for rk, off in zip(ranks, offsets)], axis=1)
+        w = np.concatenate([rk["weights"] for rk in ranks], axis=1)
+        zero = np.zeros_like(ranks[0]["shared"])
+        routed = orc.moe_finalize(x, idx.astype(np.int32), w, wkind, 2.5, zero)["out"]
+        shared = sum(bf16_bits_to_f32(rk["shared"]).astype(np.float64) for rk in ranks)
+        m = routed + shared
+        s = m + bf16_bits_to_f32(res)
+        assert np.allclose(got["out"], m, rtol=1e-13, atol=1e-13), (R, wkind)
+        assert np.allclose(got["residual_out"], s, rtol=1e-13, atol=1e-13), (R, wkind)
+        assert np.allclose(got["norm_out"], _torch_rms_norm(s, gamma, eps), rtol=1e-12,
+                           atol=1e-13), (R, wkind)
+
+
+def pin_ar_rank_order(orc):
+    """The sum over ranks does not depend on which rank is which."""
+    ranks = _rand_ranks(21, 4)
+    _, _, _, _, res, gamma = _rand_problem(21, T=4, K=3, H=24, with_norm=True)
+    a = orc.moe_finalize_ar(ranks, "fp32", 1.5, res, gamma, 1e-6)
+    b = orc.moe_finalize_ar([ranks[i] for i in (2, 0, 3, 1)], "fp32", 1.5, res, gamma, 1e-6)
+    for key in a:
+        assert np.allclose(a[key], b[key], rtol=1e-13, atol=1e-13), key
+
+
+def pin_ar_tensor_parallel_split(orc):
+    """Splitting one rank's expert rows and shared output into R equal
+    shares (exact: R is a power of two) over R ranks with the same routing
+    gives the one-rank result: the all-reduce sums, it does not average."""
+    x, idx, w, shared, res, gamma = _rand_problem(31, T=5, K=4, H=40, with_norm=True)
+    one = orc.moe_finalize(x, idx, w, "fp32", 2.5, shared, res, gamma, 1e-6)
+    for R in (2, 4, 8):
+        share = lambda b: _bits(bf16_bits_to_f32(b).astype(np.float64) / R)
+        assert np.array_equal(bf16_bits_to_f32(share(x)) * R, bf16_bits_to_f32(x))
+        ranks = [{"permuted_out": share(x), "idx": idx, "weights": w, "shared": share(shared)}
+                 for _ in range(R)]
+        got = orc.moe_finalize_ar(ranks, "fp32", 2.5, res, gamma, 1e-6)
+        for key in one:
+            assert np.allclose(got[key], one[key], rtol=1e-13, atol=1e-13), (R, key)
+
+
+def pin_ar_bad_index(orc):
+    """Each rank's indices are checked against that rank's own row count."""
+    ranks = _rand_ranks(41, 2, P=12)       # rank 0 has 12 rows, rank 1 has 15
+    ranks[1]["idx"] = ranks[1]["idx"].copy()
+    ranks[1]["idx"][0, 0] = 14             # valid on rank 1 only
+    orc.moe_finalize_ar(ranks, "fp32", 1.0)      # the valid maps are accepted
+    for r, bad in ((0, 12), (1, 15), (1, -1), (0, -1)):
+        rr = [dict(rk) for rk in ranks]
+        j = rr[r]["idx"].copy()
+        j[1, 2] = bad
+        rr[r]["idx"] = j
+        try:
+            orc.moe_finalize_ar(rr, "fp32", 1.0)
+        except ValueError:
+            continue
+        raise AssertionError(f"rank {r} index {bad} accepted")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

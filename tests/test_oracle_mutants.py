@@ -53,6 +53,25 @@ MUTANTS = [
 ]
 
 
+# the all-reduce-fused finalize (oref_moe_finalize_ar)
+AR_MUTANTS = [
+    ("ar_drop_last_rank", "for (int64_t r = 0; r < R; ++r) {\n                double partial",
+     "for (int64_t r = 0; r < R - 1; ++r) {\n                double partial"),
+    ("ar_rank0_rows_everywhere", "const uint16_t *row = permuted_out[r] +",
+     "const uint16_t *row = permuted_out[0] +"),
+    ("ar_rank0_map_everywhere", "(int64_t)idx[r][t * K + k] * H", "(int64_t)idx[0][t * K + k] * H"),
+    ("ar_rank0_weights_everywhere", "decode_weight(weights[r], wkind", "decode_weight(weights[0], wkind"),
+    ("ar_shared_of_rank0_only", "partial += bf16_to_double(shared[r][t * H + h]);",
+     "if (r == 0) partial += bf16_to_double(shared[0][t * H + h]);"),
+    ("ar_mean_not_sum", "m += partial;", "m += partial / (double)R;"),
+    ("ar_residual_per_rank", "m += partial;",
+     "m += partial + (residual && r > 0 ? bf16_to_double(residual[t * H + h]) : 0.0);"),
+    ("ar_scale_on_shared_too", "partial += bf16_to_double(shared[r][t * H + h]);",
+     "partial += routed_scale * bf16_to_double(shared[r][t * H + h]);"),
+    ("ar_bound_of_rank0", "(int64_t)idx[r][i] >= P[r]", "(int64_t)idx[r][i] >= P[0]"),
+]
+
+
 ROUTING_MUTANTS = [
     ("route_ties_keep_higher_id", "if (best < 0 || z[e] > z[best])",
      "if (best < 0 || z[e] >= z[best])"),
@@ -64,7 +83,8 @@ ROUTING_MUTANTS = [
     ("pack_array_swaps_operands", "packed[i] = oref_pack_topk_id(expert_ids[i], weights[i]);",
      "packed[i] = oref_pack_topk_id((int32_t)weights[i], (float)expert_ids[i]);"),
 ]
-ALL = [(n, o, r, 0) for n, o, r in MUTANTS] + [(n, o, r, 1) for n, o, r in ROUTING_MUTANTS]
+ALL = ([(n, o, r, 0) for n, o, r in MUTANTS + AR_MUTANTS] +
+       [(n, o, r, 1) for n, o, r in ROUTING_MUTANTS])
 
 
 @pytest.mark.parametrize("name,old,new,which", ALL, ids=[m[0] for m in ALL])
