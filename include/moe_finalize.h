@@ -286,6 +286,137 @@ moef_status moe_finalize_unfused_noalloc(const void *permuted_out, int64_t P,
                                          int T, int K, int H, cudaStream_t stream);
 
 /*
+ * ---------------------------------------------------------------------------
+ * The finalize fused with the tensor-parallel all-reduce, residual add and
+ * RMSNorm ("[Kimi K2.5] Fuse deferred MoE finalize into next-layer AR +
+ * residual + RMSNorm", Summary: weighted expert combine + shared-expert add
+ * + all-reduce + residual + RMSNorm in one kernel, keeping residual_out;
+ * Numerics & speed: the all-reduce is over the finalized token rows, and the
+ * separate-finalize fallback reaches the same result as a finalize followed
+ * by an all-reduce fused with residual + RMSNorm).
+ *
+ * R ranks of one tensor-parallel group each hold their own expert rows, row
+ * map, routing weights and shared-expert output, each a partial sum over the
+ * rank's slice of the weights.  Every rank computes, per token t:
+ *
+ *   p_r          = sum_k (w_r[t,k] * routed_scale) * permuted_out_r[idx_r[t,k], :]
+ *                  + shared_out_r[t, :]                       (fp32)
+ *   m            = p_0 + p_1 + ... + p_{R-1}                  (fp32, rank order)
+ *   out          = bf16(m)
+ *   residual_out = bf16(m + residual),  norm_out as for moe_finalize
+ *
+ * The partials are summed in fp32, in the order of the rank array, so every
+ * rank that passes the ranks in the same order obtains bit-identical
+ * outputs, and the two forms below give bit-identical results.
+ *
+ * Two forms, for two ways of ordering the ranks' work:
+ *   one-shot  moe_finalize_allreduce: one launch reads every rank's rows
+ *             directly (local or peer-mapped memory) and writes this rank's
+ *             outputs;
+ *   two-phase moe_finalize_partial on every rank (p_r in fp32, into a
+ *             buffer the other ranks can read), then, once all partials are
+ *             complete, moe_finalize_allreduce_reduce on every rank.
+ *
+ * Cross-device ordering is the caller's: the library never waits on another
+ * device.  Every pointer given for a rank must be addressable from the
+ * current device (its own memory, or a peer's mapped through peer access or
+ * IPC); everything a call reads must be complete before its launch on
+ * `stream` (e.g. cudaStreamWaitEvent on an event each rank records after its
+ * producer), and no rank may overwrite a buffer until every rank's call that
+ * reads it has finished.  No multicast memory is used.
+ * ---------------------------------------------------------------------------
+ */
+
+/* Largest tensor-parallel group the all-reduce-fused finalize serves. */
+#define MOEF_MAX_RANKS 8
+
+/* One rank's operands of the all-reduce-fused finalize, as for moe_finalize:
+ * permuted_out bf16 [P, H] (P >= 1 rows; padding rows are never read),
+ * idx_map int32 [T, K] with every entry in [0, P), weights [T, K] in the
+ * call's encoding, shared_out bf16 [T, H]. */
+typedef struct {
+    const void *permuted_out;
+    int64_t P;
+    const int32_t *idx_map;
+    const void *weights;
+    const void *shared_out;
+} moef_rank_inputs;
+
+/*
+ * moe_finalize_allreduce -- the one-shot form.  ranks: a HOST array of R
+ * moef_rank_inputs (1 <= R <= MOEF_MAX_RANKS; read during the call only).
+ * wkind, routed_scale: for every rank.  residual, gamma, eps, out,
+ * residual_out, norm_out, T, K, H: as for moe_finalize (one residual, the
+ * same on every rank; out may be NULL only with a residual).  In place:
+ * residual_out may equal residual; no other overlap.  Alignment rules as for
+ * moe_finalize, per rank.  The launch reads R * K gathered rows per token.
+ * Errors: MOEF_ERR_SHAPE for R outside [1, MOEF_MAX_RANKS] or a size out of
+ * range; otherwise as for moe_finalize.
+ */
+moef_status moe_finalize_allreduce(const moef_rank_inputs *ranks, int R,
+                                   moef_weight_kind wkind, float routed_scale,
+                                   const void *residual, const void *gamma, float eps,
+                                   void *out, void *residual_out, void *norm_out,
+                                   int T, int K, int H, cudaStream_t stream);
+
+/*
+ * moe_finalize_partial -- phase 1 of the two-phase form: this rank's p_r
+ * (see above), written unrounded as fp32 [T, H] into `partial` (4-byte
+ * aligned; 16-byte aligned with H % 8 == 0 for the vector path; not
+ * overlapping an input).  Other arguments as for moe_finalize without a
+ * residual.  The partial is read by every rank's phase 2.
+ */
+moef_status moe_finalize_partial(const void *permuted_out, int64_t P,
+                                 const int32_t *idx_map,
+                                 const void *weights, moef_weight_kind wkind,
+                                 float routed_scale, const void *shared_out,
+                                 float *partial, int T, int K, int H, cudaStream_t stream);
+
+/*
+ * moe_finalize_allreduce_reduce -- phase 2: m = sum of the R fp32 partials
+ * [T, H] in array order, then out / residual_out / norm_out exactly as
+ * moe_finalize_allreduce writes them.  partials: a HOST array of R device
+ * pointers (1 <= R <= MOEF_MAX_RANKS), each 4-byte aligned.  Other arguments
+ * as for moe_finalize_allreduce.
+ */
+moef_status moe_finalize_allreduce_reduce(const float *const *partials, int R,
+                                          const void *residual, const void *gamma, float eps,
+                                          void *out, void *residual_out, void *norm_out,
+                                          int T, int H, cudaStream_t stream);
+
+/*
+ * Launch plan of the all-reduce-fused kernels.  A CTA holds `lanes` groups
+ * of `nvc` threads (threads = lanes * nvc); in one pass thread j of group r
+ * obtains rank r's partial of vector j of the CTA's slice, and group 0 sums
+ * the ranks and finishes the vector.  Each token row is cut into `splits`
+ * slices of `slice` vectors of `vec` values, taken in `passes` passes; with
+ * a residual and splits > 1 the CTAs of a token form a cluster of `cluster`
+ * CTAs.  smem_bytes: dynamic shared memory per CTA.
+ */
+typedef struct {
+    int vec;
+    int lanes;
+    int nvc;
+    int threads;
+    int splits;
+    int slice;
+    int passes;
+    int cluster;
+    int smem_bytes;
+    int64_t grid;
+} moef_ar_plan;
+
+/*
+ * moe_finalize_allreduce_plan -- the plan of the one-shot and phase-2 calls
+ * (lanes = R; the two share it, which keeps their results bit-identical),
+ * or of phase 1 with R = 1 and with_norm = 0.  Pure host computation.
+ * Returns MOEF_ERR_SHAPE when an RMSNorm row is too long for one cluster
+ * (more than 16 CTAs x 8 passes), else as moe_finalize_plan.
+ */
+moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int vec_ok,
+                                        int num_sms, moef_ar_plan *plan);
+
+/*
  * Routing gate: the producer of the routing weights the finalize consumes
  * ("[Deepseek V4] Keep fp32 routing weights in the mxfp4 trtllm MoE",
  * description: a fused gate kernel yields fp32 routing weights, and a

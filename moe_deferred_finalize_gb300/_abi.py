@@ -43,6 +43,26 @@ class Plan(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class RankInputs(ctypes.Structure):
+    """moef_rank_inputs: one rank's operands of the all-reduce-fused finalize."""
+    _fields_ = [("permuted_out", ctypes.c_void_p), ("P", ctypes.c_int64),
+                ("idx_map", ctypes.c_void_p), ("weights", ctypes.c_void_p),
+                ("shared_out", ctypes.c_void_p)]
+
+
+class ArPlan(ctypes.Structure):
+    _fields_ = [("vec", ctypes.c_int), ("lanes", ctypes.c_int), ("nvc", ctypes.c_int),
+                ("threads", ctypes.c_int), ("splits", ctypes.c_int), ("slice", ctypes.c_int),
+                ("passes", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("grid", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+MAX_RANKS = 8       # MOEF_MAX_RANKS
+
+
 _LIB = None
 
 
@@ -69,6 +89,18 @@ def _lib():
         lib.moe_finalize_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
                                           ctypes.POINTER(Plan)]
         lib.moe_finalize_plan.restype = i32
+        lib.moe_finalize_allreduce.argtypes = [ctypes.POINTER(RankInputs), i32, i32, f32, vp, vp,
+                                               f32, vp, vp, vp, i32, i32, i32, vp]
+        lib.moe_finalize_allreduce.restype = i32
+        lib.moe_finalize_partial.argtypes = [vp, i64, vp, vp, i32, f32, vp, vp, i32, i32, i32,
+                                             vp]
+        lib.moe_finalize_partial.restype = i32
+        lib.moe_finalize_allreduce_reduce.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32, vp,
+                                                      vp, f32, vp, vp, vp, i32, i32, vp]
+        lib.moe_finalize_allreduce_reduce.restype = i32
+        lib.moe_finalize_allreduce_plan.argtypes = [i32, i32, i32, i32, i32, i32,
+                                                    ctypes.POINTER(ArPlan)]
+        lib.moe_finalize_allreduce_plan.restype = i32
         lib.moe_topk_route.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
         lib.moe_topk_route.restype = i32
         lib.pack_topk_ids.argtypes = [vp, vp, i64, vp, vp]
@@ -422,6 +454,182 @@ def plan(T: int, K: int, H: int, with_norm: bool, vec_ok: bool = True, num_sms: 
                                   threads, ctypes.byref(p))
     if st != 0:
         raise MoefError(st, "moe_finalize_plan")
+    return p.as_dict()
+
+
+# ------------------------------------------ all-reduce-fused finalize
+
+
+def _check_peer(t, name, dtypes, shape):
+    """A rank's operand: a contiguous CUDA tensor on any device (a peer's
+    buffer must be reachable from the calling device; that is the caller's
+    set-up)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if shape is not None and t.shape != shape:
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _epilogue(T, H, device, residual, gamma, out, residual_out, norm_out, write_out, like):
+    """Checks (and allocates) the residual / RMSNorm operands and outputs."""
+    norm = residual is not None
+    if norm != (gamma is not None):
+        raise ValueError("residual and gamma go together")
+    if norm:
+        _check(residual, "residual", _BF16, (T, H), device)
+        _check(gamma, "gamma", _BF16, (H,), device)
+        if residual_out is None:
+            residual_out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        if norm_out is None:
+            norm_out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        _check(residual_out, "residual_out", _BF16, (T, H), device)
+        _check(norm_out, "norm_out", _BF16, (T, H), device)
+    elif residual_out is not None or norm_out is not None:
+        raise ValueError("residual_out / norm_out need a residual")
+    if not norm or write_out:
+        if out is None:
+            out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        _check(out, "out", _BF16, (T, H), device)
+    else:
+        out = None
+    res = {"out": out}
+    if norm:
+        res["residual_out"] = residual_out
+        res["norm_out"] = norm_out
+    return res
+
+
+def _call_device(device, *candidates):
+    if device is not None:
+        return torch.device(device)
+    for t in candidates:
+        if isinstance(t, torch.Tensor) and t.is_cuda:
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def moe_finalize_allreduce(ranks, wkind: str, *, routed_scale: float = 1.0,
+                           residual: Optional[torch.Tensor] = None,
+                           gamma: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                           out: Optional[torch.Tensor] = None,
+                           residual_out: Optional[torch.Tensor] = None,
+                           norm_out: Optional[torch.Tensor] = None, write_out: bool = True,
+                           device=None, stream=None) -> dict:
+    """One-shot all-reduce-fused finalize (include/moe_finalize.h).
+
+    ranks: a list of R dicts, in rank order, with "permuted_out" bf16
+    [P_r, H], "idx_map" int32 [T, K], "weights" [T, K] (encoding ``wkind``)
+    and "shared_out" bf16 [T, H]; CUDA tensors reachable from the calling
+    device.  The residual, gamma and outputs are on the calling device
+    (``device``, else the residual's or out's device, else the current one).
+    Returns a dict like ``moe_finalize``.  Every rank's operands must be
+    complete before the launch on the stream (the caller orders devices)."""
+    if wkind not in WKIND:
+        raise ValueError(f"wkind must be one of {sorted(WKIND)}")
+    R = len(ranks)
+    if not 1 <= R <= MAX_RANKS:
+        raise ValueError(f"1 <= R <= {MAX_RANKS} ranks")
+    dev = _call_device(device, residual, out, residual_out)
+    x0, i0 = ranks[0]["permuted_out"], ranks[0]["idx_map"]
+    if x0.dim() != 2 or i0.dim() != 2:
+        raise ValueError("permuted_out is [P, H] and idx_map is [T, K]")
+    H = x0.shape[1]
+    T, K = i0.shape
+    arr = (RankInputs * R)()
+    for r, rk in enumerate(ranks):
+        x = rk["permuted_out"]
+        _check_peer(x, f"ranks[{r}].permuted_out", _BF16, None)
+        if x.dim() != 2 or x.shape[1] != H:
+            raise ValueError(f"ranks[{r}].permuted_out must be [P, {H}]")
+        _check_peer(rk["idx_map"], f"ranks[{r}].idx_map", (torch.int32,), (T, K))
+        _check_peer(rk["weights"], f"ranks[{r}].weights", _WDTYPE[wkind], (T, K))
+        _check_peer(rk["shared_out"], f"ranks[{r}].shared_out", _BF16, (T, H))
+        arr[r] = RankInputs(x.data_ptr(), x.shape[0], rk["idx_map"].data_ptr(),
+                            rk["weights"].data_ptr(), rk["shared_out"].data_ptr())
+    res = _epilogue(T, H, dev, residual, gamma, out, residual_out, norm_out, write_out, x0)
+    with _on(dev):
+        st = _lib().moe_finalize_allreduce(
+            arr, R, WKIND[wkind], float(routed_scale), _ptr(residual), _ptr(gamma), float(eps),
+            _ptr(res["out"]), _ptr(res.get("residual_out")), _ptr(res.get("norm_out")),
+            T, K, H, _stream(stream, dev))
+    if st != 0:
+        raise MoefError(st, "moe_finalize_allreduce")
+    return res
+
+
+def moe_finalize_partial(permuted_out: torch.Tensor, idx_map: torch.Tensor,
+                         weights: torch.Tensor, wkind: str, shared_out: torch.Tensor, *,
+                         routed_scale: float = 1.0, partial: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """Phase 1 of the two-phase all-reduce-fused finalize: this rank's
+    unrounded partial (weighted rows + shared output) as fp32 [T, H]
+    (allocated when not given).  Arguments as for ``moe_finalize``."""
+    if wkind not in WKIND:
+        raise ValueError(f"wkind must be one of {sorted(WKIND)}")
+    device = permuted_out.device
+    if device.type != "cuda" or permuted_out.dim() != 2 or idx_map.dim() != 2:
+        raise ValueError("permuted_out is a CUDA [P, H] tensor and idx_map is [T, K]")
+    P, H = permuted_out.shape
+    T, K = idx_map.shape
+    _check(permuted_out, "permuted_out", _BF16, (P, H), device)
+    _check(idx_map, "idx_map", (torch.int32,), (T, K), device)
+    _check(weights, "weights", _WDTYPE[wkind], (T, K), device)
+    _check(shared_out, "shared_out", _BF16, (T, H), device)
+    if partial is None:
+        partial = torch.empty((T, H), dtype=torch.float32, device=device)
+    _check(partial, "partial", (torch.float32,), (T, H), device)
+    with _on(device):
+        st = _lib().moe_finalize_partial(_ptr(permuted_out), P, _ptr(idx_map), _ptr(weights),
+                                         WKIND[wkind], float(routed_scale), _ptr(shared_out),
+                                         _ptr(partial), T, K, H, _stream(stream, device))
+    if st != 0:
+        raise MoefError(st, "moe_finalize_partial")
+    return partial
+
+
+def moe_finalize_allreduce_reduce(partials, *, residual: Optional[torch.Tensor] = None,
+                                  gamma: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                                  out: Optional[torch.Tensor] = None,
+                                  residual_out: Optional[torch.Tensor] = None,
+                                  norm_out: Optional[torch.Tensor] = None,
+                                  write_out: bool = True, device=None, stream=None) -> dict:
+    """Phase 2: sum the ranks' fp32 partials [T, H] (a list in rank order,
+    CUDA tensors reachable from the calling device), then the residual add
+    and RMSNorm; outputs as for ``moe_finalize_allreduce`` and bit-identical
+    to it."""
+    R = len(partials)
+    if not 1 <= R <= MAX_RANKS:
+        raise ValueError(f"1 <= R <= {MAX_RANKS} partials")
+    if partials[0].dim() != 2:
+        raise ValueError("partials are [T, H]")
+    T, H = partials[0].shape
+    for r, t in enumerate(partials):
+        _check_peer(t, f"partials[{r}]", (torch.float32,), (T, H))
+    dev = _call_device(device, residual, out, residual_out)
+    res = _epilogue(T, H, dev, residual, gamma, out, residual_out, norm_out, write_out, None)
+    arr = (ctypes.c_void_p * R)(*[t.data_ptr() for t in partials])
+    with _on(dev):
+        st = _lib().moe_finalize_allreduce_reduce(
+            arr, R, _ptr(residual), _ptr(gamma), float(eps), _ptr(res["out"]),
+            _ptr(res.get("residual_out")), _ptr(res.get("norm_out")), T, H, _stream(stream, dev))
+    if st != 0:
+        raise MoefError(st, "moe_finalize_allreduce_reduce")
+    return res
+
+
+def allreduce_plan(R: int, T: int, H: int, with_norm: bool, vec_ok: bool = True,
+                   num_sms: int = 152) -> dict:
+    """The launch plan of the one-shot and phase-2 calls (phase 1: R = 1,
+    with_norm = False); host computation only."""
+    p = ArPlan()
+    st = _lib().moe_finalize_allreduce_plan(R, T, H, int(with_norm), int(vec_ok), num_sms,
+                                            ctypes.byref(p))
+    if st != 0:
+        raise MoefError(st, "moe_finalize_allreduce_plan")
     return p.as_dict()
 
 

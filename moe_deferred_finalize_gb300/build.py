@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_finalize.so")
-SOURCES = ["finalize.cu", "unfused.cu", "routing.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["finalize.cu", "allreduce.cu", "unfused.cu", "routing.cu", "api.cu", "noalloc.cu"]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3",
               "-std=c++17", "-Xcompiler", "-fPIC,-O2,-Wall", "-I", INCLUDE, "-I", CSRC]

@@ -1,0 +1,328 @@
+// The deferred finalize of R tensor-parallel ranks, summed over the ranks,
+// then the residual add and RMSNorm ("[Kimi K2.5] Fuse deferred MoE finalize
+// into next-layer AR + residual + RMSNorm", Summary: weighted expert combine
+// + shared-expert add + all-reduce + residual + RMSNorm in one kernel, with
+// residual_out kept; Numerics & speed: the same result from a standalone
+// finalize followed by an all-reduce fused with residual + RMSNorm):
+//
+//   p_r = sum_k (w_r[t,k] * routed_scale) * x_r[idx_r[t,k], :] + shared_r[t, :]
+//   m   = p_0 + p_1 + ... + p_{R-1}          (in rank order, fp32)
+//   out = bf16(m);  residual_out = bf16(m + residual);
+//   norm_out = bf16(residual_out * rsqrt(mean(residual_out^2) + eps) * gamma)
+//
+// One kernel template serves three entry points:
+//   * one-shot (moe_finalize_allreduce): every rank's rows are gathered in
+//     one launch, from local or peer-mapped memory;
+//   * phase 1 (moe_finalize_partial): one rank's p_r, stored in fp32;
+//   * phase 2 (moe_finalize_allreduce_reduce): the fp32 partials of all
+//     ranks summed, then the epilogue.
+// The one-shot and the two-phase forms run the same arithmetic in the same
+// order under the same launch plan, so their results are bit-identical.
+//
+// Thread layout: a CTA's threads form `lanes` groups of `nvc` threads, group
+// r working for rank r (lanes = R; 1 in phase 1).  In one pass thread (r, j)
+// obtains rank r's partial of vector j of the CTA's slice (K gathered-row
+// loads, 16 bytes each, plus the shared-output load; or the fp32 partial),
+// so a pass keeps R times as many loads in flight as one thread summing all
+// ranks would.  The partials meet in shared memory and the threads of group
+// 0 add them in rank order and finish the vector.  With RMSNorm the bf16
+// residual_out vectors stay in shared memory for the second pass, and a
+// split row combines its partial sums of squares across the CTAs of a
+// thread-block cluster through distributed shared memory, as in the plain
+// finalize.
+//
+// Launch order: a programmatic dependent of the previous kernel on the
+// stream (griddepcontrol.wait before any global memory access); it lets the
+// next kernel begin launching once its loads are done.  No thread spins.
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+
+#include "internal.cuh"
+#include "vec.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace moef {
+namespace {
+
+constexpr int kArMaxThreads = 512;
+constexpr int kArMaxCluster = 16;
+constexpr int kMaxSlots = MOEF_MAX_RANKS * MOEF_MAX_K;
+
+// fp32 vectors of the partials: 8 values as two 16-byte accesses, or one.
+template <int VEC>
+struct F32Ops;
+
+template <>
+struct F32Ops<8> {
+    static __device__ __forceinline__ void load(const float *p, float f[8]) {
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+        const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+    static __device__ __forceinline__ void store(float *p, const float f[8]) {
+        reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+};
+
+template <>
+struct F32Ops<1> {
+    static __device__ __forceinline__ void load(const float *p, float f[1]) { f[0] = __ldcs(p); }
+    static __device__ __forceinline__ void store(float *p, const float f[1]) { p[0] = f[0]; }
+};
+
+// PASSES: with RMSNorm, the number of passes over the slice (1, 2, 4 or 8),
+// fixed so that the gamma vectors can be held in registers; 0 without
+// RMSNorm (any number of passes).
+template <int VEC, bool NORM, bool CLUSTER, int PASSES>
+__global__ void __launch_bounds__(kArMaxThreads, 2)
+finalize_ar_kernel(const __grid_constant__ ArParams p) {
+    using Ops = VecOps<VEC>;
+    using FOps = F32Ops<VEC>;
+    using V = typename Ops::V;
+
+    __shared__ const uint16_t *s_row[kMaxSlots];   // [rank][slot]
+    __shared__ float s_w[kMaxSlots];
+    __shared__ float s_warp[kArMaxThreads / 32];
+    __shared__ float s_part[kArMaxCluster];
+    // dynamic: the ranks' partials of one pass, float [lanes][nvc][VEC]
+    // (lanes > 1), then with RMSNorm the kept residual_out vectors, V [PASSES][nvc]
+    extern __shared__ __align__(16) unsigned char s_dyn[];
+    const int lanes = p.lanes;
+    const int nvc = p.nvc;
+    float *s_p = reinterpret_cast<float *>(s_dyn);
+    V *s_keep = reinterpret_cast<V *>(s_dyn + (lanes > 1 ? sizeof(float) * VEC * lanes * nvc : 0));
+
+    if constexpr (CLUSTER) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+    const int r = threadIdx.x / nvc;        // the rank this thread works for
+    const int j = threadIdx.x - r * nvc;    // its vector within a pass
+    const int S = p.splits;
+    const int t = blockIdx.x / S;
+    const int split = blockIdx.x - t * S;
+    const int K = p.K;
+    const int64_t tok = static_cast<int64_t>(t) * p.H;
+    const int v_begin = split * p.slice;
+    const int v_end = min(v_begin + p.slice, p.nvec);
+    const bool gather = p.reduce == 0;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (gather) {
+        // every rank's row pointers and scaled weights for this token
+        const int nslots = lanes * K;
+        for (int i = threadIdx.x; i < nslots; i += blockDim.x) {
+            const int rr = i / K;
+            const int64_t slot = static_cast<int64_t>(t) * K + (i - rr * K);
+            const int row = __ldg(p.idx[rr] + slot);
+            s_row[i] = p.x[rr] + static_cast<int64_t>(row) * p.H;
+            s_w[i] = decode_weight(p.weights[rr], p.wkind, slot) * p.routed_scale;
+        }
+    }
+    // the finishing threads' first residual vector does not depend on the
+    // staged pointers: its load goes out before the staging barrier
+    V rs_first;
+    if (NORM && r == 0 && v_begin + j < v_end)
+        rs_first = Ops::load(p.residual + tok + static_cast<int64_t>(v_begin + j) * VEC);
+    __syncthreads();
+
+    float ss = 0.f;
+    int q = 0;
+    for (int base = v_begin; base < v_end; base += nvc, ++q) {
+        const int v = base + j;
+        const bool active = v < v_end;
+        const int64_t e = static_cast<int64_t>(v) * VEC;
+        float acc[VEC];
+        if (active) {
+            if (gather) {
+                const V sh = Ops::load(p.shared[r] + tok + e);
+                const uint16_t *const *rows = s_row + r * K;
+                const float *ws = s_w + r * K;
+#pragma unroll
+                for (int u = 0; u < VEC; ++u) acc[u] = 0.f;
+                for (int k0 = 0; k0 < K; k0 += 8) {
+                    V xv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (k0 + u < K) xv[u] = Ops::load_row(rows[k0 + u] + e);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (k0 + u < K) {
+                            float xf[VEC];
+                            Ops::to_f32(xv[u], xf);
+                            const float w = ws[k0 + u];
+#pragma unroll
+                            for (int c = 0; c < VEC; ++c) acc[c] = fmaf(w, xf[c], acc[c]);
+                        }
+                    }
+                }
+                float f[VEC];
+                Ops::to_f32(sh, f);
+#pragma unroll
+                for (int c = 0; c < VEC; ++c) acc[c] += f[c];
+            } else {
+                FOps::load(p.partial[r] + tok + e, acc);
+            }
+        }
+        if (lanes > 1) {
+            float *mine = s_p + (static_cast<int64_t>(r) * nvc + j) * VEC;
+            if (active) {
+#pragma unroll
+                for (int c = 0; c < VEC; ++c) mine[c] = acc[c];
+            }
+            __syncthreads();
+            if (r == 0 && active) {
+                for (int rr = 1; rr < lanes; ++rr) {
+                    const float *other = s_p + (static_cast<int64_t>(rr) * nvc + j) * VEC;
+#pragma unroll
+                    for (int c = 0; c < VEC; ++c) acc[c] += other[c];
+                }
+            }
+            if (base + nvc < v_end) __syncthreads();   // s_p is refilled by the next pass
+        }
+        if (r == 0 && active) {
+            if (p.partial_out) {
+                FOps::store(p.partial_out + tok + e, acc);
+            } else {
+                if (p.out) Ops::store(p.out + tok + e, Ops::from_f32(acc));
+                if constexpr (NORM) {
+                    const V rs = (q == 0) ? rs_first : Ops::load(p.residual + tok + e);
+                    float f[VEC];
+                    Ops::to_f32(rs, f);
+#pragma unroll
+                    for (int c = 0; c < VEC; ++c) acc[c] += f[c];
+                    const V sv = Ops::from_f32(acc);
+                    Ops::store(p.residual_out + tok + e, sv);
+                    s_keep[q * nvc + j] = sv;
+                    Ops::to_f32(sv, f);
+#pragma unroll
+                    for (int c = 0; c < VEC; ++c) ss = fmaf(f[c], f[c], ss);
+                }
+            }
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if constexpr (NORM) {
+        V g[PASSES];
+#pragma unroll
+        for (int qq = 0; qq < PASSES; ++qq) {
+            const int v = v_begin + qq * nvc + j;
+            if (r == 0 && v < v_end) g[qq] = Ops::load_reused(p.gamma + static_cast<int64_t>(v) * VEC);
+        }
+        ss = warp_sum(ss);
+        if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
+        __syncthreads();
+        float total = 0.f;
+        const int nw = (blockDim.x + 31) >> 5;
+        for (int w = 0; w < nw; ++w) total += s_warp[w];
+
+        if constexpr (CLUSTER) {
+            // each CTA pushes its partial into slot [own rank] of every CTA of
+            // the cluster, then one release/acquire cluster barrier
+            cg::cluster_group cluster = cg::this_cluster();
+            const unsigned own = cluster.block_rank();
+            asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+            if (threadIdx.x < static_cast<unsigned>(S))
+                *cluster.map_shared_rank(&s_part[own], static_cast<int>(threadIdx.x)) = total;
+            cluster.sync();
+            total = 0.f;
+            for (int c = 0; c < S; ++c) total += s_part[c];
+        }
+
+        const float inv = rsqrtf(total / static_cast<float>(p.H) + p.eps);
+        if (r == 0) {
+#pragma unroll
+            for (int qq = 0; qq < PASSES; ++qq) {
+                const int v = v_begin + qq * nvc + j;
+                if (v < v_end) {
+                    float sf[VEC], gf[VEC];
+                    Ops::to_f32(s_keep[qq * nvc + j], sf);
+                    Ops::to_f32(g[qq], gf);
+#pragma unroll
+                    for (int c = 0; c < VEC; ++c) sf[c] = sf[c] * inv * gf[c];
+                    Ops::store(p.norm_out + tok + static_cast<int64_t>(v) * VEC, Ops::from_f32(sf));
+                }
+            }
+        }
+    }
+}
+
+template <int VEC, bool NORM, bool CLUSTER, int PASSES>
+cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream) {
+    auto kern = finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES>;
+    cudaLaunchAttribute attr[2];
+    unsigned num_attrs = 0;
+    attr[num_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[num_attrs].val.programmaticStreamSerializationAllowed = 1;
+    ++num_attrs;
+    if (CLUSTER) {
+        if (plan.cluster > 8) {
+            // clusters of 9..16 CTAs are opt-in per kernel and device
+            static std::atomic<int> enabled[64];
+            int dev = 0;
+            cudaError_t err = cudaGetDevice(&dev);
+            if (err != cudaSuccess) return err;
+            if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+            if (!enabled[dev].load(std::memory_order_relaxed)) {
+                err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (err != cudaSuccess) return err;
+                enabled[dev].store(1, std::memory_order_relaxed);
+            }
+        }
+        attr[num_attrs].id = cudaLaunchAttributeClusterDimension;
+        attr[num_attrs].val.clusterDim.x = static_cast<unsigned>(plan.cluster);
+        attr[num_attrs].val.clusterDim.y = 1;
+        attr[num_attrs].val.clusterDim.z = 1;
+        ++num_attrs;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(plan.threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = num_attrs;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int VEC, bool CLUSTER>
+cudaError_t launch_ar_norm(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream) {
+    switch (plan.passes) {
+        case 1: return launch_ar_t<VEC, true, CLUSTER, 1>(p, plan, stream);
+        case 2: return launch_ar_t<VEC, true, CLUSTER, 2>(p, plan, stream);
+        case 4: return launch_ar_t<VEC, true, CLUSTER, 4>(p, plan, stream);
+        case 8: return launch_ar_t<VEC, true, CLUSTER, 8>(p, plan, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int VEC>
+cudaError_t launch_ar_vec(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream) {
+    if (!p.residual) return launch_ar_t<VEC, false, false, 0>(p, plan, stream);
+    if (plan.cluster > 1) return launch_ar_norm<VEC, true>(p, plan, stream);
+    return launch_ar_norm<VEC, false>(p, plan, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_finalize_ar(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream) {
+    // the plan must match the parameters it is launched with: one group of
+    // nvc threads per lane, and with RMSNorm every vector of the slice
+    // covered within the kernel's fixed number of passes
+    if (plan.lanes != p.lanes || plan.nvc != p.nvc || plan.threads != p.lanes * p.nvc ||
+        plan.threads > kArMaxThreads || plan.splits != p.splits || plan.slice != p.slice)
+        return cudaErrorInvalidValue;
+    if (p.residual && static_cast<int64_t>(plan.passes) * plan.nvc < plan.slice)
+        return cudaErrorInvalidValue;
+    if (p.reduce == 0 && p.lanes * p.K > kMaxSlots) return cudaErrorInvalidValue;
+    if (plan.vec == 8) return launch_ar_vec<8>(p, plan, stream);
+    if (plan.vec == 1) return launch_ar_vec<1>(p, plan, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moef

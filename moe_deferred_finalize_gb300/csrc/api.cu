@@ -368,4 +368,240 @@ moef_status moe_finalize_check_indices(const int32_t *idx_map, int T, int K, int
     return cuda_status(moef::launch_check_indices(idx_map, n, P, d_bad_count, sms, stream));
 }
 
+// ---------------------------------------------------------------------------
+// All-reduce-fused finalize (kernels in allreduce.cu)
+
+namespace {
+
+constexpr int kArMaxThreads = 512;    // the all-reduce kernels' launch bounds
+constexpr int kArMaxPasses = 8;
+
+int pow2_bucket(int need) {
+    int b = 1;
+    while (b < need) b *= 2;
+    return b;
+}
+
+}  // namespace
+
+// Plan of the all-reduce-fused kernels.  A CTA holds R groups of threads,
+// one per rank, each thread obtaining one rank's partial of one vector per
+// pass, so that decode-size calls keep every rank's row loads in flight at
+// once:
+//  * without RMSNorm, 128 threads per CTA (R groups of 128 / R, at least 16
+//    threads), one vector per thread: slices of 128 / R vectors;
+//  * with RMSNorm, one CTA or one cluster of up to 16 CTAs finishes a row.
+//    Groups of up to 512 / R threads (at most 256), a multiple of 32: with
+//    R = 8 at H = 7168, 14 CTAs of 8 x 64 threads.  The split is halved while
+//    the grid exceeds 4 CTAs per SM, each thread then taking up to 8 passes.
+moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int vec_ok,
+                                        int num_sms, moef_ar_plan *plan) {
+    if (!plan) return MOEF_ERR_NULL;
+    if (R < 1 || R > MOEF_MAX_RANKS || T < 0 || H < 1) return MOEF_ERR_SHAPE;
+    if (num_sms < 1) return MOEF_ERR_ARG;
+    const int vec = (vec_ok && H % 8 == 0) ? 8 : 1;
+    const int nvec = H / vec;
+    const int64_t rows = T > 0 ? T : 1;
+    int nvc, splits, slice, passes;
+    if (!with_norm) {
+        nvc = 128 / R / 16 * 16;
+        if (nvc < 16) nvc = 16;
+        if (nvc > nvec) nvc = nvec;
+        slice = nvc;
+        splits = ceil_div(nvec, slice);
+        if (rows * splits > 0x7FFFFFFFLL) {
+            splits = static_cast<int>(0x7FFFFFFFLL / rows);
+            if (splits < 1) splits = 1;
+            slice = ceil_div(nvec, splits);
+        }
+        passes = ceil_div(slice, nvc);
+    } else {
+        int nvc_max = kArMaxThreads / R;
+        if (nvc_max > 256) nvc_max = 256;
+        nvc_max = nvc_max / 32 * 32;
+        splits = ceil_div(nvec, nvc_max);
+        if (splits > kMaxCluster) splits = kMaxCluster;
+        if (ceil_div(ceil_div(nvec, splits), nvc_max) > kArMaxPasses) return MOEF_ERR_SHAPE;
+        while (splits > 1 && rows * splits > 4 * static_cast<int64_t>(num_sms)) {
+            const int half = ceil_div(splits, 2);
+            if (ceil_div(ceil_div(nvec, half), nvc_max) > kArMaxPasses) break;
+            splits = half;
+        }
+        slice = ceil_div(nvec, splits);
+        passes = pow2_bucket(ceil_div(slice, nvc_max));
+        nvc = ceil_div(slice, passes);
+        if (nvc > 32) nvc = round_up(nvc, 32);
+        if (nvc > nvc_max) nvc = nvc_max;
+    }
+    splits = ceil_div(nvec, slice);   // no empty CTAs
+    const int64_t grid = static_cast<int64_t>(T) * splits;
+    if (grid > 0x7FFFFFFFLL) return MOEF_ERR_SHAPE;
+    const int vbytes = vec == 8 ? 16 : 2;
+    int64_t smem = (R > 1 ? static_cast<int64_t>(sizeof(float)) * vec * R * nvc : 0) +
+                   (with_norm ? static_cast<int64_t>(passes) * nvc * vbytes : 0);
+    plan->vec = vec;
+    plan->lanes = R;
+    plan->nvc = nvc;
+    plan->threads = R * nvc;
+    plan->splits = splits;
+    plan->slice = slice;
+    plan->passes = passes;
+    plan->cluster = (with_norm && splits > 1) ? splits : 1;
+    plan->smem_bytes = static_cast<int>(smem);
+    plan->grid = grid;
+    return MOEF_OK;
+}
+
+namespace {
+
+// Argument checks of the residual / RMSNorm epilogue shared by the one-shot
+// and phase-2 calls (the rules of moe_finalize).
+moef_status check_epilogue(const void *residual, const void *gamma, float eps, void *out,
+                           void *residual_out, void *norm_out) {
+    if ((residual == nullptr) != (gamma == nullptr)) return MOEF_ERR_ARG;
+    if (residual) {
+        if (!residual_out || !norm_out) return MOEF_ERR_NULL;
+        if (!(eps >= 0.f) || isinf(eps)) return MOEF_ERR_ARG;
+    } else {
+        if (residual_out || norm_out) return MOEF_ERR_ARG;
+        if (!out) return MOEF_ERR_NULL;
+    }
+    const void *ptrs[] = {residual, gamma, out, residual_out, norm_out};
+    for (const void *q : ptrs)
+        if (q && !aligned(q, 2)) return MOEF_ERR_ALIGN;
+    return MOEF_OK;
+}
+
+bool epilogue_vec_ok(const void *residual, const void *gamma, const void *out,
+                     const void *residual_out, const void *norm_out) {
+    const void *ptrs[] = {residual, gamma, out, residual_out, norm_out};
+    for (const void *q : ptrs)
+        if (q && !aligned(q, 16)) return false;
+    return true;
+}
+
+void fill_epilogue(moef::ArParams *p, const void *residual, const void *gamma, float eps,
+                   void *out, void *residual_out, void *norm_out) {
+    p->residual = static_cast<const uint16_t *>(residual);
+    p->gamma = static_cast<const uint16_t *>(gamma);
+    p->out = static_cast<uint16_t *>(out);
+    p->residual_out = static_cast<uint16_t *>(residual_out);
+    p->norm_out = static_cast<uint16_t *>(norm_out);
+    p->eps = eps;
+}
+
+// Checks one rank's gather operands; clears *vec_ok when one of them rules
+// out the 16-byte path.
+moef_status check_rank(const moef_rank_inputs &rk, moef_weight_kind wkind, bool *vec_ok) {
+    if (rk.P < 1) return MOEF_ERR_SHAPE;
+    if (!rk.permuted_out || !rk.idx_map || !rk.weights || !rk.shared_out) return MOEF_ERR_NULL;
+    if (!aligned(rk.permuted_out, 2) || !aligned(rk.shared_out, 2) || !aligned(rk.idx_map, 4) ||
+        !aligned(rk.weights, wkind == MOEF_W_BF16 ? 2 : 4))
+        return MOEF_ERR_ALIGN;
+    if (!aligned(rk.permuted_out, 16) || !aligned(rk.shared_out, 16)) *vec_ok = false;
+    return MOEF_OK;
+}
+
+moef_status launch_ar(moef::ArParams &p, int R, int T, int H, bool norm, bool vec_ok,
+                      cudaStream_t stream) {
+    int sms = 0;
+    moef_status st = cuda_status(current_sms(&sms));
+    if (st != MOEF_OK) return st;
+    moef_ar_plan plan;
+    st = moe_finalize_allreduce_plan(R, T, H, norm ? 1 : 0, vec_ok ? 1 : 0, sms, &plan);
+    if (st != MOEF_OK) return st;
+    p.H = H;
+    p.nvec = H / plan.vec;
+    p.lanes = plan.lanes;
+    p.nvc = plan.nvc;
+    p.splits = plan.splits;
+    p.slice = plan.slice;
+    return cuda_status(moef::launch_finalize_ar(p, plan, stream));
+}
+
+}  // namespace
+
+moef_status moe_finalize_allreduce(const moef_rank_inputs *ranks, int R, moef_weight_kind wkind,
+                                   float routed_scale, const void *residual, const void *gamma,
+                                   float eps, void *out, void *residual_out, void *norm_out,
+                                   int T, int K, int H, cudaStream_t stream) {
+    if (R < 1 || R > MOEF_MAX_RANKS || T < 0 || K < 1 || K > MOEF_MAX_K || H < 1)
+        return MOEF_ERR_SHAPE;
+    if (wkind != MOEF_W_FP32 && wkind != MOEF_W_BF16 && wkind != MOEF_W_PACKED_TOPK)
+        return MOEF_ERR_ARG;
+    if (T == 0) return MOEF_OK;
+    if (!ranks) return MOEF_ERR_NULL;
+    moef::ArParams p = {};
+    bool vec_ok = (H % 8) == 0;
+    for (int r = 0; r < R; ++r) {
+        moef_status st = check_rank(ranks[r], wkind, &vec_ok);
+        if (st != MOEF_OK) return st;
+        p.x[r] = static_cast<const uint16_t *>(ranks[r].permuted_out);
+        p.idx[r] = ranks[r].idx_map;
+        p.weights[r] = ranks[r].weights;
+        p.shared[r] = static_cast<const uint16_t *>(ranks[r].shared_out);
+    }
+    moef_status st = check_epilogue(residual, gamma, eps, out, residual_out, norm_out);
+    if (st != MOEF_OK) return st;
+    if (!epilogue_vec_ok(residual, gamma, out, residual_out, norm_out)) vec_ok = false;
+    fill_epilogue(&p, residual, gamma, eps, out, residual_out, norm_out);
+    p.routed_scale = routed_scale;
+    p.wkind = static_cast<int>(wkind);
+    p.K = K;
+    p.reduce = 0;
+    return launch_ar(p, R, T, H, residual != nullptr, vec_ok, stream);
+}
+
+moef_status moe_finalize_partial(const void *permuted_out, int64_t P, const int32_t *idx_map,
+                                 const void *weights, moef_weight_kind wkind, float routed_scale,
+                                 const void *shared_out, float *partial, int T, int K, int H,
+                                 cudaStream_t stream) {
+    if (T < 0 || K < 1 || K > MOEF_MAX_K || H < 1) return MOEF_ERR_SHAPE;
+    if (wkind != MOEF_W_FP32 && wkind != MOEF_W_BF16 && wkind != MOEF_W_PACKED_TOPK)
+        return MOEF_ERR_ARG;
+    if (T == 0) return MOEF_OK;
+    const moef_rank_inputs rk = {permuted_out, P, idx_map, weights, shared_out};
+    bool vec_ok = (H % 8) == 0;
+    moef_status st = check_rank(rk, wkind, &vec_ok);
+    if (st != MOEF_OK) return st;
+    if (!partial) return MOEF_ERR_NULL;
+    if (!aligned(partial, 4)) return MOEF_ERR_ALIGN;
+    if (!aligned(partial, 16)) vec_ok = false;
+    moef::ArParams p = {};
+    p.x[0] = static_cast<const uint16_t *>(permuted_out);
+    p.idx[0] = idx_map;
+    p.weights[0] = weights;
+    p.shared[0] = static_cast<const uint16_t *>(shared_out);
+    p.partial_out = partial;
+    p.routed_scale = routed_scale;
+    p.wkind = static_cast<int>(wkind);
+    p.K = K;
+    p.reduce = 0;
+    return launch_ar(p, 1, T, H, false, vec_ok, stream);
+}
+
+moef_status moe_finalize_allreduce_reduce(const float *const *partials, int R,
+                                          const void *residual, const void *gamma, float eps,
+                                          void *out, void *residual_out, void *norm_out,
+                                          int T, int H, cudaStream_t stream) {
+    if (R < 1 || R > MOEF_MAX_RANKS || T < 0 || H < 1) return MOEF_ERR_SHAPE;
+    if (T == 0) return MOEF_OK;
+    if (!partials) return MOEF_ERR_NULL;
+    moef::ArParams p = {};
+    bool vec_ok = (H % 8) == 0;
+    for (int r = 0; r < R; ++r) {
+        if (!partials[r]) return MOEF_ERR_NULL;
+        if (!aligned(partials[r], 4)) return MOEF_ERR_ALIGN;
+        if (!aligned(partials[r], 16)) vec_ok = false;
+        p.partial[r] = partials[r];
+    }
+    moef_status st = check_epilogue(residual, gamma, eps, out, residual_out, norm_out);
+    if (st != MOEF_OK) return st;
+    if (!epilogue_vec_ok(residual, gamma, out, residual_out, norm_out)) vec_ok = false;
+    fill_epilogue(&p, residual, gamma, eps, out, residual_out, norm_out);
+    p.K = 1;
+    p.reduce = 1;
+    return launch_ar(p, R, T, H, residual != nullptr, vec_ok, stream);
+}
+
 }  // extern "C"

@@ -36,6 +36,35 @@ struct FinalizeParams {
 cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan, int num_sms,
                             cudaStream_t stream);
 
+// Everything one launch of the all-reduce-fused finalize kernel needs
+// (one-shot, phase 1 or phase 2; allreduce.cu).
+struct ArParams {
+    const uint16_t *x[MOEF_MAX_RANKS];          // each rank's permuted_out, bf16 [P_r, H]
+    const int32_t *idx[MOEF_MAX_RANKS];         // each rank's [T, K] row map
+    const void *weights[MOEF_MAX_RANKS];        // each rank's [T, K] weights (wkind)
+    const uint16_t *shared[MOEF_MAX_RANKS];     // each rank's shared_out, bf16 [T, H]
+    const float *partial[MOEF_MAX_RANKS];       // phase 2: each rank's fp32 [T, H] partial
+    const uint16_t *residual;                   // bf16 [T, H] or null
+    const uint16_t *gamma;                      // bf16 [H] or null
+    uint16_t *out;                              // bf16 [T, H] or null
+    uint16_t *residual_out;                     // bf16 [T, H] or null
+    uint16_t *norm_out;                         // bf16 [T, H] or null
+    float *partial_out;                         // phase 1: fp32 [T, H], else null
+    float routed_scale;
+    float eps;
+    int wkind;
+    int K, H;
+    int nvec;                                   // vectors per row
+    int lanes;                                  // thread groups per CTA (ranks summed)
+    int nvc;                                    // threads per group = vectors per pass
+    int splits;                                 // CTAs per token
+    int slice;                                  // vectors per CTA
+    int reduce;                                 // 1: sum fp32 partials (phase 2)
+};
+
+// Launches the all-reduce-fused finalize kernel according to `plan`.
+cudaError_t launch_finalize_ar(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream);
+
 // Launches the unfused three-kernel finalize (combine into tmp, add the
 // shared output, residual + RMSNorm); `plan` is a plan without RMSNorm.
 cudaError_t launch_unfused(const FinalizeParams &p, const moef_plan &plan, uint16_t *tmp,

@@ -327,3 +327,75 @@ def make(name: str, alloc: Alloc = _np_alloc, threads: Optional[int] = None) -> 
     if name == "prefill_t16384":
         return prefill(16384, alloc=alloc, threads=threads, name=name)
     raise KeyError(name)
+
+
+# ------------------------------------------------- tensor-parallel groups
+
+
+@dataclasses.dataclass
+class TPGroup:
+    """One all-reduce-fused finalize problem: R ranks' own operands (each a
+    Workload without residual) and the residual, gamma and eps they share."""
+    name: str
+    ranks: list
+    residual: Optional[np.ndarray]   # uint16 [T, H] or None
+    gamma: Optional[np.ndarray]      # uint16 [H] or None
+    eps: float
+
+    @property
+    def R(self) -> int:
+        return len(self.ranks)
+
+    @property
+    def with_norm(self) -> bool:
+        return self.residual is not None
+
+    def __getattr__(self, item):      # T, K, H, wkind, routed_scale: as on every rank
+        if item in ("T", "K", "H", "E", "wkind", "routed_scale"):
+            return getattr(self.ranks[0], item)
+        raise AttributeError(item)
+
+
+def tp_group(name: str, R: int, T: int, K: int, H: int, E: int, tile: int, P: int, *,
+             weight_rule: str = "sigmoid", wkind: str = "fp32", routed_scale: float = 1.0,
+             with_norm: bool = True, eps: float = 1e-6, seed: int = 0,
+             require_all: bool = False, alloc: Alloc = _np_alloc,
+             threads: Optional[int] = None) -> TPGroup:
+    """R ranks of one tensor-parallel group, each with its own expert rows
+    (the rank's partial of every expert output), routing and shared-expert
+    partial, from seeds spawned off ``seed``; the residual ~ N(0, 4) and
+    gamma ~ U(0.5, 1.5) are common to all ranks.  Pool routing as for
+    ``synth`` (P rows in blocks of ``tile``)."""
+    ss = np.random.SeedSequence([seed, R])
+    rank_seeds = ss.spawn(R + 1)
+    ranks = [synth(f"{name}_rank{r}", T=T, K=K, H=H, E=E, tile=tile, P=P,
+                   weight_rule=weight_rule, wkind=wkind, routed_scale=routed_scale,
+                   require_all=require_all,
+                   seed=int(rank_seeds[r].generate_state(1)[0]), alloc=alloc, threads=threads)
+             for r in range(R)]
+    residual = gamma = None
+    if with_norm:
+        s_res, s_gamma = rank_seeds[R].spawn(2)
+        residual = alloc((T, H), np.uint16)
+        _fill_rows(residual, s_res, "normal", 0.0, 2.0, threads or 1)
+        gamma = alloc((H,), np.uint16)
+        rng_g = np.random.Generator(np.random.PCG64(s_gamma))
+        gamma[:] = to_bf16_bits(rng_g.uniform(0.5, 1.5, H))
+    return TPGroup(name=name, ranks=ranks, residual=residual, gamma=gamma, eps=eps)
+
+
+# The decode shapes of the all-reduce-fused finalize: Kimi K2.5-like
+# (H = 7168, top-8 of 384 experts) at batch 1 and 16, as in the
+# "[Kimi K2.5] Fuse deferred MoE finalize ..." page's timings, and batch 256
+# with the 6272-row permuted buffer named there.
+TP_SHAPES = {1: dict(E=384, tile=32, P=256), 16: dict(E=384, tile=64, P=2048),
+             256: dict(E=256, tile=128, P=6272)}
+
+
+def tp_decode(R: int, T: int, with_norm: bool = True, seed: int = 5,
+              alloc: Alloc = _np_alloc) -> TPGroup:
+    """R ranks at decode batch T (1, 16 or 256), H = 7168, K = 8, fp32
+    normalised-sigmoid routing, routed scale 2.5, residual + RMSNorm."""
+    shape = TP_SHAPES[T]
+    return tp_group(f"tp{R}_t{T}", R, T=T, K=8, H=7168, weight_rule="sigmoid",
+                    routed_scale=2.5, with_norm=with_norm, seed=seed, alloc=alloc, **shape)

@@ -205,6 +205,107 @@ def test_plan_invariants(mf):
                         assert p["cluster"] == 1
 
 
+def test_allreduce_argument_errors(mf):
+    """The all-reduce-fused entry points check every rank's operands and the
+    epilogue before any CUDA call."""
+    from moe_deferred_finalize_gb300 import _abi
+    OK, NUL, SHAPE, ALIGN, ARG = 0, 1, 2, 3, 4
+    lib = mf.lib()
+
+    def ranks(n, **bad):
+        arr = (_abi.RankInputs * max(n, 1))()
+        for r in range(n):
+            f = dict(permuted_out=A, P=16, idx_map=A, weights=A, shared_out=A)
+            if r == n - 1:
+                f.update(bad)
+            arr[r] = _abi.RankInputs(f["permuted_out"], f["P"], f["idx_map"], f["weights"],
+                                     f["shared_out"])
+        return arr
+
+    def ar(R=2, T=2, K=2, H=8, wkind=0, arr=None, residual=NULL, gamma=NULL, eps=1e-6,
+           out=A, residual_out=NULL, norm_out=NULL, **bad):
+        arr = ranks(R, **bad) if arr is None else arr
+        return lib.moe_finalize_allreduce(arr, R, wkind, 1.0, residual, gamma, eps, out,
+                                          residual_out, norm_out, T, K, H, NULL)
+
+    assert ar(T=0) == OK
+    for R in (0, -1, 9):
+        assert ar(R=R, arr=ranks(1)) == SHAPE
+    assert ar(K=0) == SHAPE and ar(K=33) == SHAPE and ar(H=0) == SHAPE and ar(T=-1) == SHAPE
+    assert ar(wkind=3) == ARG
+    assert lib.moe_finalize_allreduce(None, 2, 0, 1.0, NULL, NULL, 1e-6, A, NULL, NULL,
+                                      2, 2, 8, NULL) == NUL
+    assert ar(P=0) == SHAPE                      # the last rank's buffer is empty
+    for field in ("permuted_out", "idx_map", "weights", "shared_out"):
+        assert ar(**{field: NULL}) == NUL, field
+    assert ar(permuted_out=A + 1) == ALIGN
+    assert ar(shared_out=A + 1) == ALIGN
+    assert ar(idx_map=A + 2) == ALIGN
+    assert ar(weights=A + 2) == ALIGN            # fp32 weights need 4 bytes
+    assert ar(wkind=1, weights=A + 2) != ALIGN   # bf16 weights need 2
+    assert ar(out=NULL) == NUL
+    assert ar(residual=A) == ARG and ar(gamma=A) == ARG
+    assert ar(residual=A, gamma=A) == NUL
+    assert ar(residual_out=A) == ARG
+    assert ar(residual=A, gamma=A, residual_out=A, norm_out=A, eps=-1.0) == ARG
+    assert ar(out=A + 1) == ALIGN
+
+    part = lib.moe_finalize_partial
+    assert part(A, 16, A, A, 0, 1.0, A, A, 0, 2, 8, NULL) == OK
+    assert part(A, 16, A, A, 0, 1.0, A, NULL, 2, 2, 8, NULL) == NUL
+    assert part(A, 16, A, A, 0, 1.0, A, A + 2, 2, 2, 8, NULL) == ALIGN
+    assert part(A, 0, A, A, 0, 1.0, A, A, 2, 2, 8, NULL) == SHAPE
+    assert part(A, 16, A, A, 5, 1.0, A, A, 2, 2, 8, NULL) == ARG
+    assert part(NULL, 16, A, A, 0, 1.0, A, A, 2, 2, 8, NULL) == NUL
+
+    red = lib.moe_finalize_allreduce_reduce
+    parts = (ctypes.c_void_p * 3)(A, A, A)
+    assert red(parts, 3, NULL, NULL, 1e-6, A, NULL, NULL, 0, 8, NULL) == OK
+    assert red(parts, 0, NULL, NULL, 1e-6, A, NULL, NULL, 2, 8, NULL) == SHAPE
+    assert red(parts, 9, NULL, NULL, 1e-6, A, NULL, NULL, 2, 8, NULL) == SHAPE
+    assert red(None, 3, NULL, NULL, 1e-6, A, NULL, NULL, 2, 8, NULL) == NUL
+    assert red((ctypes.c_void_p * 3)(A, NULL, A), 3, NULL, NULL, 1e-6, A, NULL, NULL,
+               2, 8, NULL) == NUL
+    assert red((ctypes.c_void_p * 3)(A, A + 2, A), 3, NULL, NULL, 1e-6, A, NULL, NULL,
+               2, 8, NULL) == ALIGN
+    assert red(parts, 3, A, NULL, 1e-6, A, NULL, NULL, 2, 8, NULL) == ARG
+    assert red(parts, 3, NULL, NULL, 1e-6, NULL, NULL, NULL, 2, 8, NULL) == NUL
+
+
+def test_allreduce_plans(mf):
+    """Plan invariants over ranks, sizes and both epilogues: R groups of
+    threads per CTA, every vector of a row covered, and with RMSNorm one
+    cluster of at most 16 CTAs and at most 8 passes per thread."""
+    for R in range(1, 9):
+        for H in (8, 64, 100, 1000, 2048, 4104, 7168, 16384, 65536):
+            for T in (1, 16, 256, 4096):
+                for norm in (False, True):
+                    for vec_ok in (True, False):
+                        try:
+                            p = mf.allreduce_plan(R, T, H, norm, vec_ok)
+                        except mf.MoefError as e:
+                            assert e.status == 2 and norm
+                            continue
+                        nvec = H // p["vec"]
+                        assert p["lanes"] == R and p["threads"] == R * p["nvc"] <= 512
+                        assert p["splits"] * p["slice"] >= nvec > (p["splits"] - 1) * p["slice"]
+                        assert p["passes"] * p["nvc"] >= p["slice"]
+                        assert p["grid"] == T * p["splits"]
+                        if norm:
+                            assert p["passes"] in (1, 2, 4, 8)
+                            assert p["cluster"] == p["splits"] <= 16
+                        else:
+                            assert p["cluster"] == 1
+                        assert p["smem_bytes"] <= 48 * 1024
+    # the decode shapes: every rank's loads of a vector in flight in one pass
+    p = mf.allreduce_plan(8, 1, 7168, True)
+    assert (p["nvc"], p["splits"], p["passes"], p["cluster"]) == (64, 14, 1, 14)
+    with pytest.raises(mf.MoefError):
+        mf.allreduce_plan(8, 1, 8 * 8 * 16 * 64 + 8, True)    # longer than 16 CTAs x 8 passes
+    with pytest.raises(mf.MoefError):
+        mf.allreduce_plan(9, 1, 7168, True)
+
+
 def test_every_accepted_norm_plan_covers_its_slice_in_one_pass(mf):
     """The RMSNorm kernel makes one pass over its slice, and its launcher
     refuses a plan that leaves vectors without a thread; so every plan the
