@@ -225,15 +225,47 @@ def device_inputs(wl, device):
     return d
 
 
-def call(mf, wl, d, outs, stream=None, routing_ready=False):
+def call(mf, wl, d, outs, stream=None, routing_ready=False, pdl=True):
     mf.moe_finalize(d["x"], d["idx"], d["w"], wl.wkind, d["shared"],
                     routed_scale=wl.routed_scale, residual=d.get("residual"),
                     gamma=d.get("gamma"), eps=wl.eps, out=outs.get("out"),
                     residual_out=outs.get("residual_out"), norm_out=outs.get("norm_out"),
-                    write_out="out" in outs, routing_ready=routing_ready, stream=stream)
+                    write_out="out" in outs, routing_ready=routing_ready, pdl=pdl,
+                    stream=stream)
 
 
-def time_headline(mf, wl, d, outs, steps, warmup, ws, device, sampler=None):
+def graph_us(fn, device, calls, n_pass, reps=5):
+    """µs per call of ``fn`` (which enqueues ``calls`` calls) captured once in
+    a CUDA graph and replayed ``n_pass`` times per repetition; median of
+    ``reps`` repetitions timed with CUDA events on the replaying stream."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    cur = torch.cuda.current_stream(device)
+    cur.wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    samples = []
+    for _ in range(reps):
+        a.record(cur)
+        for _ in range(n_pass):
+            g.replay()
+        b.record(cur)
+        torch.cuda.synchronize(device)
+        samples.append(a.elapsed_time(b) * 1e3 / (n_pass * calls))
+    del g
+    return statistics.median(samples)
+
+
+def time_headline(mf, wl, d, outs, steps, warmup, ws, device):
+    """The timed steps: ``warmup`` untimed calls, then ``steps`` back-to-back
+    calls between a barrier and a synchronize on each side.  Returns (total
+    ms from the first step's start event to the last step's end event,
+    per-step ms, host wall-clock window)."""
     stream = torch.cuda.current_stream(device)
     for _ in range(warmup):
         call(mf, wl, d, outs)
@@ -249,16 +281,49 @@ def time_headline(mf, wl, d, outs, steps, warmup, ws, device, sampler=None):
         b.record(stream)
     torch.cuda.synchronize(device)
     t1 = time.time()
-    if sampler is not None:
-        sampler.mark(t0, t1)
     barrier(ws)
     per = [a.elapsed_time(b) for a, b in ev]
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
-    return total_ms, per
+    return total_ms, per, (t0, t1)
 
 
-def decode_latency(mf, name, device, reps):
-    """µs per call on inputs rotated through copies whose total exceeds L2."""
+def time_roofline(mf, wl, d, outs, device, min_seconds):
+    """Per-launch CUDA-event durations of back-to-back headline launches on
+    the launching stream, for at least ``min_seconds`` of GPU time (so that
+    the clock sampler sees many samples whatever --steps is).  Returns
+    (durations in ms, host wall-clock window)."""
+    stream = torch.cuda.current_stream(device)
+    probe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(10)]
+    for a, b in probe:
+        a.record(stream)
+        call(mf, wl, d, outs)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    est_ms = statistics.median(a.elapsed_time(b) for a, b in probe)
+    n = int(max(200, np.ceil(min_seconds * 1e3 / max(est_ms, 1e-3))))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    for a, b in ev:
+        a.record(stream)
+        call(mf, wl, d, outs)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    return [a.elapsed_time(b) for a, b in ev], (t0, t1)
+
+
+def decode_latency(mf, name, device, reps, peak, producer=False):
+    """µs per call on inputs rotated through copies whose total exceeds L2.
+
+    With ``producer``: also the µs the finalize adds behind a kernel that
+    writes its row buffer, as in an MoE layer where the expert GEMM has just
+    written permuted_out: (producer + finalize) - (producer alone) per call,
+    both as CUDA-graph replays, with the finalize launched as a programmatic
+    dependent (the default), as a plain stream-ordered kernel, and with
+    MOEF_FLAG_ROUTING_READY."""
     wl = W.make(name)
     d = device_inputs(wl, device)
     norm = wl.with_norm
@@ -326,43 +391,78 @@ def decode_latency(mf, name, device, reps):
         return statistics.median(samples)
 
     def graph(fn):
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream(device)
-        s.wait_stream(torch.cuda.current_stream(device))
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s):
-                fn()
-        torch.cuda.current_stream(device).wait_stream(s)
-        g.replay()
-        torch.cuda.synchronize(device)
-        samples = []
-        for _ in range(5):
-            a.record()
-            for _ in range(n_pass):
-                g.replay()
-            b.record()
-            torch.cuda.synchronize(device)
-            samples.append(a.elapsed_time(b) * 1e3 / (n_pass * R))
-        del g
-        return statistics.median(samples)
+        return graph_us(fn, device, R, n_pass)
 
     eager_checked_us = eager(one_pass)      # argument checks on every call
     eager_us = eager(one_pass_bound)        # checked once, then raw C-ABI calls
-    graph_us = graph(one_pass)
+    graph_us_ = graph(one_pass)
     ready_us = graph(one_pass_ready)
     unfused_us = graph(one_pass_unfused)
     warm_us = graph(one_pass_warm)
-    plan = mf.plan(wl.T, wl.K, wl.H, norm, True,
-                   torch.cuda.get_device_properties(device).multi_processor_count)
+    res = {"T": wl.T, "K": wl.K, "H": wl.H, "routing": wl.wkind, "rmsnorm": norm,
+           "us_per_call_graph": round(graph_us_, 3), "us_per_call_eager": round(eager_us, 3),
+           "us_per_call_eager_checked": round(eager_checked_us, 3),
+           "us_per_call_graph_routing_ready": round(ready_us, 3),
+           "unfused_us_per_call_graph": round(unfused_us, 3),
+           "us_per_call_graph_rows_in_l2": round(warm_us, 3),
+           "bytes_per_call": touched,
+           "GBps_graph": round(touched / (graph_us_ * 1e-6) / 1e9, 1),
+           "frac": round(touched / (graph_us_ * 1e-6) / 1e9 / peak, 4),
+           "us_bytes_at_peak": round(touched / (peak * 1e9) * 1e6, 3),
+           "copies": R, "calls": n_pass * R,
+           "plan": mf.plan(wl.T, wl.K, wl.H, norm, True,
+                           torch.cuda.get_device_properties(device).multi_processor_count)}
+
+    if producer:
+        # Two producers rewrite each copy's row buffer [P, H] just before its
+        # call, reading a source buffer of the same size:
+        #  * a plain elementwise kernel, which never signals its dependents
+        #    early (griddepcontrol.launch_dependents), like most library
+        #    kernels (not a copy: a copy would be captured as a memcpy node);
+        #  * a kernel that does signal them after its loads, as a producer
+        #    written for programmatic dependent launch would: this library's
+        #    finalize with K = 1 and zero weights, so that out = the source.
+        src = d["x"].clone()
+        zero_idx = torch.zeros((wl.P, 1), dtype=torch.int32, device=device)
+        zero_w = torch.zeros((wl.P, 1), dtype=torch.float32, device=device)
+
+        def plain(dd):
+            torch.mul(src, 1.0, out=dd["x"])
+
+        def pdl_aware(dd):
+            mf.moe_finalize(src[:1], zero_idx, zero_w, "fp32", src, out=dd["x"])
+
+        def prod(kind):
+            def f():
+                for dd, _ in sets:
+                    kind(dd)
+            return f
+
+        def prod_then(kind, **kw):
+            def f():
+                for dd, oo in sets:
+                    kind(dd)
+                    call(mf, wl, dd, oo, **kw)
+            return f
+
+        res["us_added_after_producer"] = {}
+        res["producer_us_per_call_graph"] = {}
+        for name, kind in (("plain_kernel", plain), ("pdl_aware_kernel", pdl_aware)):
+            alone = graph(prod(kind))
+            added = {"pdl": graph(prod_then(kind)) - alone,
+                     "no_pdl": graph(prod_then(kind, pdl=False)) - alone,
+                     "routing_ready": graph(prod_then(kind, routing_ready=True)) - alone}
+            res["producer_us_per_call_graph"][name] = round(alone, 3)
+            res["us_added_after_producer"][name] = {k: round(v, 3) for k, v in added.items()}
+        res["producer"] = (f"a kernel writing the whole [{wl.P}, {wl.H}] bf16 row buffer "
+                           f"({wl.P * wl.H * 2} bytes) from a source of the same size just "
+                           f"before each call; plain_kernel: torch elementwise multiply by 1; "
+                           f"pdl_aware_kernel: moe_finalize with K=1 and zero weights "
+                           f"(out = shared = the source), which signals its dependents after "
+                           f"its loads")
+        del src, zero_idx, zero_w
     del xs, shs, rss, outs, bound, ws
-    return {"T": wl.T, "K": wl.K, "H": wl.H, "routing": wl.wkind, "rmsnorm": norm,
-            "us_per_call_graph": round(graph_us, 3), "us_per_call_eager": round(eager_us, 3),
-            "us_per_call_eager_checked": round(eager_checked_us, 3),
-            "us_per_call_graph_routing_ready": round(ready_us, 3),
-            "unfused_us_per_call_graph": round(unfused_us, 3),
-            "us_per_call_graph_rows_in_l2": round(warm_us, 3),
-            "GBps_graph": round(touched / (graph_us * 1e-6) / 1e9, 1),
-            "copies": R, "calls": n_pass * R, "plan": plan}
+    return res
 
 
 def gate_latency(mf, device, T, E=256, K=8, calls=2000):
@@ -411,6 +511,120 @@ def gate_latency(mf, device, T, E=256, K=8, calls=2000):
         samples.append(a.elapsed_time(b) * 1e3 / (n_pass * R))
     del g, z, outs
     return round(statistics.median(samples), 3)
+
+
+def allreduce_bytes(R, T, K, H, wbytes=4):
+    """Algorithmic bytes of one one-shot all-reduce-fused call that writes
+    residual_out and norm_out: every rank's gathered rows, shared output and
+    routing once, the residual once, the two outputs, gamma."""
+    return R * (T * K * H * 2 + T * H * 2 + T * K * (4 + wbytes)) + 3 * T * H * 2 + H * 2
+
+
+def allreduce_latency(mf, device, R, T, peak, calls=1000):
+    """µs per call of the all-reduce-fused finalize at decode size T over R
+    ranks' buffer sets on this one GPU (CUDA-graph replay, every call on
+    buffer copies no other call in the pass touched, the copies together
+    larger than L2):
+
+      * one-shot: one launch reading every rank's rows (what each rank
+        would run, with the peers' rows read over NVLink instead of HBM);
+      * two-phase, one rank: phase 1 for its own partial, then phase 2 over
+        all R partials (the other R - 1 already in place);
+      * phase 1 and phase 2 alone;
+      * the plain finalize of one rank's operands with residual + RMSNorm,
+        for comparison with R of them."""
+    g = W.tp_decode(R, T)
+    K, H = g.K, g.H
+    nbytes = allreduce_bytes(R, T, K, H)
+    C = int(min(max(2, np.ceil(2 * L2_BYTES / nbytes)), 512))
+
+    def rep(a):   # C copies at distinct addresses
+        t = host_tensor(np.ascontiguousarray(a)).to(device)
+        return t.unsqueeze(0).expand(C, *t.shape).contiguous()
+
+    ranks = [{"permuted_out": rep(wl.permuted_out), "idx_map": rep(wl.idx),
+              "weights": rep(wl.weights), "shared_out": rep(wl.shared)} for wl in g.ranks]
+    res_in, gamma = rep(g.residual), host_tensor(g.gamma).to(device)
+    r_out = torch.empty((C, T, H), dtype=torch.bfloat16, device=device)
+    n_out = torch.empty_like(r_out)
+    partials = torch.empty((C, R, T, H), dtype=torch.float32, device=device)
+    sets = [([{k: v[c] for k, v in rk.items()} for rk in ranks],
+             dict(residual=res_in[c], gamma=gamma, eps=g.eps, residual_out=r_out[c],
+                  norm_out=n_out[c], write_out=False), partials[c]) for c in range(C)]
+    scale = g.routed_scale
+
+    def oneshot():
+        for rks, ep, _ in sets:
+            mf.moe_finalize_allreduce(rks, g.wkind, routed_scale=scale, **ep)
+
+    def phase1(rks, part):
+        r0 = rks[0]
+        mf.moe_finalize_partial(r0["permuted_out"], r0["idx_map"], r0["weights"], g.wkind,
+                                r0["shared_out"], routed_scale=scale, partial=part[0])
+
+    def two_phase_rank():
+        for rks, ep, part in sets:
+            phase1(rks, part)
+            mf.moe_finalize_allreduce_reduce(list(part), **ep)
+
+    def phase1_only():
+        for rks, _, part in sets:
+            phase1(rks, part)
+
+    def phase2_only():
+        for _, ep, part in sets:
+            mf.moe_finalize_allreduce_reduce(list(part), **ep)
+
+    def standalone():
+        for rks, ep, _ in sets:
+            r0 = rks[0]
+            mf.moe_finalize(r0["permuted_out"], r0["idx_map"], r0["weights"], g.wkind,
+                            r0["shared_out"], routed_scale=scale, **ep)
+
+    for rks, _, part in sets:                 # every partial in place once
+        for r, rk in enumerate(rks):
+            mf.moe_finalize_partial(rk["permuted_out"], rk["idx_map"], rk["weights"], g.wkind,
+                                    rk["shared_out"], routed_scale=scale, partial=part[r])
+    oneshot()
+    torch.cuda.synchronize(device)
+    n_pass = max(1, calls // C)
+    t = {name: graph_us(fn, device, C, n_pass)
+         for name, fn in (("one_shot", oneshot), ("two_phase_rank", two_phase_rank),
+                          ("phase1", phase1_only), ("phase2", phase2_only),
+                          ("standalone_finalize", standalone))}
+    out = {f"us_{k}": round(v, 3) for k, v in t.items()}
+    out.update({"R": R, "T": T, "K": K, "H": H, "bytes_one_shot": nbytes,
+                "GBps_one_shot": round(nbytes / (t["one_shot"] * 1e-6) / 1e9, 1),
+                "frac_one_shot": round(nbytes / (t["one_shot"] * 1e-6) / 1e9 / peak, 4),
+                "us_R_x_standalone_finalize": round(R * t["standalone_finalize"], 3),
+                "copies": C, "calls": n_pass * C,
+                "plan": mf.allreduce_plan(R, T, H, True)})
+    del ranks, res_in, r_out, n_out, partials, sets
+    torch.cuda.empty_cache()
+    return out
+
+
+def link_gbs(device, h2d_bytes, d2h_bytes, reps=5):
+    """Plain pinned-memory copy rates of the host link for the given byte
+    counts: one H2D copy and one D2H copy each, median of ``reps``."""
+    res = {}
+    for name, nb in (("h2d", h2d_bytes), ("d2h", d2h_bytes)):
+        host = torch.empty(nb, dtype=torch.uint8, pin_memory=True)
+        dev = torch.empty(nb, dtype=torch.uint8, device=device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        samples = []
+        for _ in range(reps + 1):
+            a.record()
+            if name == "h2d":
+                dev.copy_(host, non_blocking=True)
+            else:
+                host.copy_(dev, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize(device)
+            samples.append(nb / (a.elapsed_time(b) * 1e-3) / 1e9)
+        res[name] = round(statistics.median(samples[1:]), 1)
+        del host, dev
+    return res
 
 
 def e2e_zero_copy(mf, wl, host, device, steps):
@@ -528,6 +742,47 @@ def oracle_times(wl, want_out, reps=3, min_seconds=0.0):
     return statistics.median(single), statistics.median(parallel), threads
 
 
+def oracle_allreduce_seconds(R, T):
+    """Seconds of one single-threaded fp64 oracle pass over the R-rank
+    decode problem at batch T (the all-reduce-fused finalize)."""
+    import oracle   # test infrastructure: timed here, never used by the GPU path
+    g = W.tp_decode(R, T)
+    ranks = [{"permuted_out": wl.permuted_out, "idx": wl.idx, "weights": wl.weights,
+              "shared": wl.shared} for wl in g.ranks]
+    t0 = time.perf_counter()
+    oracle.default().moe_finalize_ar(ranks, g.wkind, g.routed_scale, g.residual, g.gamma,
+                                     g.eps, want_out=False)
+    return time.perf_counter() - t0
+
+
+CONFIG_KEYS = {"tiny": "T4_tiny", "decode_bs1_packed": "T1", "decode_bs256": "T256",
+               "fused_norm_bs16": "T16_rmsnorm"}
+
+
+def per_config_summary(decode, kernel_ms, achieved, peak, nbytes, cpu):
+    """µs per call, GB/s, fraction of the HBM peak and the oracle's times for
+    each of the five workloads, side by side."""
+    out = {}
+    wms = (cpu or {}).get("workloads_ms", {})
+    for name, key in CONFIG_KEYS.items():
+        dd = decode.get(key)
+        if not dd:
+            continue
+        out[name] = {"us_per_call": dd["us_per_call_graph"], "GBps": dd["GBps_graph"],
+                     "frac": dd["frac"], "us_bytes_at_peak": dd["us_bytes_at_peak"],
+                     "floor_us_dependent_launch": dd["floor_us_dependent_launch"],
+                     "timing": "CUDA-graph replay, inputs rotated over copies larger than L2"}
+    out[WORKLOAD] = {"us_per_call": round(kernel_ms * 1e3, 2), "GBps": round(achieved, 1),
+                     "frac": round(achieved / peak, 4),
+                     "us_bytes_at_peak": round(nbytes / (peak * 1e9) * 1e6, 2),
+                     "timing": "mean CUDA-event duration of back-to-back launches"}
+    for name, v in out.items():
+        if name in wms:
+            v["oracle_ms_one_thread"] = wms[name]["one_thread"]
+            v["oracle_ms_all_cores"] = wms[name]["all_cores"]
+    return out
+
+
 # Which outputs each workload writes in the benchmark (the prefill emits
 # residual_out and norm_out only; every other workload writes out as well).
 def writes_out(name, wl):
@@ -588,12 +843,15 @@ def run_ours(args, ws, rank, local):
     sampler = ClockSampler(device.index if device.index is not None else 0)
     if rank == 0:
         sampler.start()
-    total_ms, per = time_headline(mf, wl, d, outs, args.steps, args.warmup, ws, device,
-                                  sampler if rank == 0 else None)
+    total_ms, per, (win0, _) = time_headline(mf, wl, d, outs, args.steps, args.warmup, ws,
+                                             device)
+    roof_ms, (_, win1) = time_roofline(mf, wl, d, outs, device, args.roofline_seconds)
+    if rank == 0:
+        sampler.mark(win0, win1)     # the timed steps and the roofline launches
     clocks = sampler.stop() if rank == 0 else None
 
     ms_step = max_over_ranks(total_ms / args.steps, ws)
-    kernel_ms = statistics.mean(per)
+    kernel_ms = statistics.mean(roof_ms)
     value = sum_over_ranks(nbytes, ws) / (ms_step * 1e-3) / 1e9
 
     peak, peak_src = measured_peaks()
@@ -612,19 +870,31 @@ def run_ours(args, ws, rank, local):
     e2e_value = sum_over_ranks(nbytes, ws) / (e2e_ms * 1e-3) / 1e9
     c_ms, c_h2d, c_d2h = e2e_copy(mf, wl, host, device, e2e_steps)
     c_ms = max_over_ranks(c_ms, ws)
+    link = link_gbs(device, h2d, d2h)
     torch.cuda.empty_cache()
     decode = {}
     if not args.skip_decode:
-        decode = {"T1": decode_latency(mf, "decode_bs1_packed", device, 4000),
-                  "T256": decode_latency(mf, "decode_bs256", device, 2000),
-                  "T16_rmsnorm": decode_latency(mf, "fused_norm_bs16", device, 2000),
-                  "T4_tiny": decode_latency(mf, "tiny", device, 2000)}
+        decode = {"T1": decode_latency(mf, "decode_bs1_packed", device, 4000, peak,
+                                       producer=True),
+                  "T256": decode_latency(mf, "decode_bs256", device, 2000, peak, producer=True),
+                  "T16_rmsnorm": decode_latency(mf, "fused_norm_bs16", device, 2000, peak,
+                                                producer=True),
+                  "T4_tiny": decode_latency(mf, "tiny", device, 2000, peak)}
+        floor = decode["T4_tiny"]["us_per_call_graph"]
+        for v in decode.values():
+            v["floor_us_dependent_launch"] = floor
 
     gate = {}
     if not args.skip_decode:
         gate = {"E": 256, "K": 8, "kind": "sigmoid", "outputs": "ids, fp32 weights, packed",
                 "us_per_call_graph": {f"T{T}": gate_latency(mf, device, T)
                                       for T in (1, 256, 16384)}}
+
+    allreduce = {}
+    if not args.skip_decode:
+        for R in (1, 2, 4, 8):
+            for T in (1, 16, 256):
+                allreduce[f"R{R}_T{T}"] = allreduce_latency(mf, device, R, T, peak)
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -647,6 +917,12 @@ def run_ours(args, ws, rank, local):
             s1, sn, _ = oracle_times(cw, want_out=writes_out(name, cw))
             cpu["workloads_ms"][name] = {"one_thread": round(1e3 * s1, 3),
                                          "all_cores": round(1e3 * sn, 3)}
+        if allreduce:
+            cpu["allreduce_ms_one_thread"] = {
+                key: round(1e3 * oracle_allreduce_seconds(v["R"], v["T"]), 3)
+                for key, v in allreduce.items()}
+
+    configs = per_config_summary(decode, kernel_ms, achieved, peak, nbytes, cpu)
 
     if rank != 0:
         return 0
@@ -669,20 +945,28 @@ def run_ours(args, ws, rank, local):
                                    "over copies larger than L2"} if decode else None),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": peak_src, "kernel_ms": round(kernel_ms, 5)},
+                     "peak_source": peak_src, "kernel_ms": round(kernel_ms, 5),
+                     "launches": len(roof_ms),
+                     "window_s": round(sum(roof_ms) * 1e-3, 3),
+                     "sm_mhz_median": clocks.get("sm_mhz") if clocks else None},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": round(e2e_ms, 3),
                 "mode": "moe_finalize_host: pinned host inputs read and pinned host outputs "
-                        "written by the kernel over the host link, no separate copies"},
+                        "written by the kernel over the host link, no separate copies",
+                "link_gbs": link,
+                "link_ms_per_step": round(h2d / (link["h2d"] * 1e9) * 1e3, 3),
+                "frac_of_link": round(h2d / (link["h2d"] * 1e9) * 1e3 / e2e_ms, 4)},
         "e2e_copy": {"value": round(sum_over_ranks(nbytes, ws) / (c_ms * 1e-3) / 1e9, 1),
                      "unit": "GB/s", "h2d_bytes_per_step": c_h2d, "d2h_bytes_per_step": c_d2h,
                      "steps": e2e_steps, "ms_per_step": round(c_ms, 3),
                      "mode": "H2D copies of all inputs, call on device buffers, D2H copies"},
         "clocks": clocks,
         "gpu_launches": args.steps,
+        "configs": configs,
         "decode": decode,
         "gate": gate,
+        "allreduce": allreduce,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -696,6 +980,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-decode", action="store_true", help="omit the decode latency lines")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU oracle baseline")
+    ap.add_argument("--roofline-seconds", type=float, default=2.0,
+                    help="GPU seconds of back-to-back launches behind roofline.kernel_ms")
     ap.add_argument("--ref-budget-s", type=float, default=60.0,
                     help="--impl reference: seconds of oracle work over all steps")
     args = ap.parse_args(argv)

@@ -198,6 +198,16 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok,
 #define MOEF_FLAG_ROUTING_READY 1u
 
 /*
+ * MOEF_FLAG_NO_PDL: launch the kernel as a plain stream-ordered kernel, not
+ * as a programmatic dependent of the previous kernel: its launch and CTA
+ * set-up then wait for the previous kernel to complete instead of
+ * overlapping its tail.  Results are the same.  For callers whose previous
+ * kernel must not share the GPU with the finalize's CTAs, and to measure
+ * what the dependent launch saves.
+ */
+#define MOEF_FLAG_NO_PDL 2u
+
+/*
  * moe_finalize_ex -- moe_finalize with launch hints (0 = automatic), for
  * callers that pin a launch shape (e.g. one captured graph for several
  * batch sizes) and for tuning, and with `flags` (MOEF_FLAG_*, 0 = none;

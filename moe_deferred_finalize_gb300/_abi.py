@@ -216,11 +216,12 @@ def _empty_like(t, device):
 
 
 FLAG_ROUTING_READY = 1
+FLAG_NO_PDL = 2
 
 
 def _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale, residual, gamma,
              eps, out, residual_out, norm_out, write_out, splits, threads, host=False,
-             routing_ready=False):
+             routing_ready=False, pdl=True):
     """Validate, allocate missing outputs; returns (C arguments, outputs).
     host=True: every tensor is a pinned CPU tensor, used in place."""
     if wkind not in WKIND:
@@ -262,7 +263,7 @@ def _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale, re
     args = (_ptr(permuted_out), P, _ptr(idx_map), _ptr(weights), WKIND[wkind],
             float(routed_scale), _ptr(shared_out), _ptr(residual), _ptr(gamma), float(eps),
             _ptr(out), _ptr(residual_out), _ptr(norm_out), T, K, H, int(splits), int(threads),
-            FLAG_ROUTING_READY if routing_ready else 0)
+            (FLAG_ROUTING_READY if routing_ready else 0) | (0 if pdl else FLAG_NO_PDL))
     res = {"out": out}
     if norm:
         res["residual_out"] = residual_out
@@ -277,7 +278,7 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
                  residual_out: Optional[torch.Tensor] = None,
                  norm_out: Optional[torch.Tensor] = None, write_out: bool = True,
                  splits: int = 0, threads: int = 0, routing_ready: bool = False,
-                 stream=None) -> dict:
+                 pdl: bool = True, stream=None) -> dict:
     """Deferred MoE finalize on the GPU (see include/moe_finalize.h).
 
     permuted_out bf16 [P, H]; idx_map int32 [T, K]; weights [T, K] encoded
@@ -288,11 +289,12 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
     with "out" and, with a residual, "residual_out" and "norm_out".
     Enqueued on the current stream (or ``stream``); nothing is synchronised.
     ``routing_ready``: idx_map and weights were complete before the previous
-    kernel on the stream started (MOEF_FLAG_ROUTING_READY).
+    kernel on the stream started (MOEF_FLAG_ROUTING_READY).  ``pdl=False``:
+    launch as a plain stream-ordered kernel (MOEF_FLAG_NO_PDL).
     """
     args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
                          residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
-                         threads, routing_ready=routing_ready)
+                         threads, routing_ready=routing_ready, pdl=pdl)
     device = permuted_out.device
     with _on(device):
         st = _call_ex(args, _stream(stream, device))
@@ -436,13 +438,13 @@ def bind(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: torch.Tenso
          eps: float = 1e-6, out: Optional[torch.Tensor] = None,
          residual_out: Optional[torch.Tensor] = None, norm_out: Optional[torch.Tensor] = None,
          write_out: bool = True, splits: int = 0, threads: int = 0,
-         routing_ready: bool = False, stream=None) -> BoundFinalize:
+         routing_ready: bool = False, pdl: bool = True, stream=None) -> BoundFinalize:
     """Check and marshal a finalize once (arguments as for ``moe_finalize``);
     the returned object enqueues it on ``stream`` (default: the current
     stream at bind time) each time it is called."""
     args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
                          residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
-                         threads, routing_ready=routing_ready)
+                         threads, routing_ready=routing_ready, pdl=pdl)
     return BoundFinalize(args, res, stream, permuted_out.device)
 
 

@@ -75,11 +75,29 @@ struct F32Ops<1> {
     static __device__ __forceinline__ void store(float *p, const float f[1]) { p[0] = f[0]; }
 };
 
+// Rank r's entry of a per-rank pointer array of the kernel parameters.  Each
+// entry is read with a compile-time index (a constant-bank operand) and the
+// rank's one selected, instead of indexing the parameter array with a
+// run-time rank, which would turn every such read into a dependent load.
+template <typename T>
+__device__ __forceinline__ T rank_entry(const T (&a)[MOEF_MAX_RANKS], int r) {
+    T v = a[0];
+#pragma unroll
+    for (int i = 1; i < MOEF_MAX_RANKS; ++i)
+        if (r == i) v = a[i];
+    return v;
+}
+
 // PASSES: with RMSNorm, the number of passes over the slice (1, 2, 4 or 8),
 // fixed so that the gamma vectors can be held in registers; 0 without
 // RMSNorm (any number of passes).
-template <int VEC, bool NORM, bool CLUSTER, int PASSES>
-__global__ void __launch_bounds__(kArMaxThreads, 2)
+// MINB: CTAs of 512 threads that must fit one SM.  2 (64 registers) for
+// grids above one CTA per SM, where resident warps hide latency; 1 (up to
+// 128 registers) for smaller grids, whose time is a chain of memory
+// latencies: there the registers let every gathered load of a vector go out
+// before the first FMA, while 64 registers with RMSNorm spill and split them.
+template <int VEC, bool NORM, bool CLUSTER, int PASSES, int MINB>
+__global__ void __launch_bounds__(kArMaxThreads, MINB)
 finalize_ar_kernel(const __grid_constant__ ArParams p) {
     using Ops = VecOps<VEC>;
     using FOps = F32Ops<VEC>;
@@ -109,6 +127,10 @@ finalize_ar_kernel(const __grid_constant__ ArParams p) {
     const int v_begin = split * p.slice;
     const int v_end = min(v_begin + p.slice, p.nvec);
     const bool gather = p.reduce == 0;
+    // this thread's rank's dense operand: its shared output (gather) or its
+    // fp32 partial (phase 2)
+    const void *dense_r = gather ? static_cast<const void *>(rank_entry(p.shared, r))
+                                 : static_cast<const void *>(rank_entry(p.partial, r));
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -118,16 +140,27 @@ finalize_ar_kernel(const __grid_constant__ ArParams p) {
         for (int i = threadIdx.x; i < nslots; i += blockDim.x) {
             const int rr = i / K;
             const int64_t slot = static_cast<int64_t>(t) * K + (i - rr * K);
-            const int row = __ldg(p.idx[rr] + slot);
-            s_row[i] = p.x[rr] + static_cast<int64_t>(row) * p.H;
-            s_w[i] = decode_weight(p.weights[rr], p.wkind, slot) * p.routed_scale;
+            const int row = __ldg(rank_entry(p.idx, rr) + slot);
+            s_row[i] = rank_entry(p.x, rr) + static_cast<int64_t>(row) * p.H;
+            s_w[i] = decode_weight(rank_entry(p.weights, rr), p.wkind, slot) * p.routed_scale;
         }
     }
-    // the finishing threads' first residual vector does not depend on the
-    // staged pointers: its load goes out before the staging barrier
-    V rs_first;
-    if (NORM && r == 0 && v_begin + j < v_end)
-        rs_first = Ops::load(p.residual + tok + static_cast<int64_t>(v_begin + j) * VEC);
+    // The first pass's dense operands do not depend on the staged pointers:
+    // their loads go out before the staging barrier, beside the row-map
+    // loads (the finishing threads' residual; in the small-grid build, whose
+    // time is a chain of latencies and which has the registers for it, also
+    // this thread's rank's shared output or fp32 partial).
+    constexpr bool kHoist = MINB == 1;
+    V sh_first, rs_first;
+    float part_first[VEC];
+    if (v_begin + j < v_end) {
+        const int64_t e = static_cast<int64_t>(v_begin + j) * VEC;
+        if (kHoist && gather)
+            sh_first = Ops::load(static_cast<const uint16_t *>(dense_r) + tok + e);
+        else if (kHoist)
+            FOps::load(static_cast<const float *>(dense_r) + tok + e, part_first);
+        if (NORM && r == 0) rs_first = Ops::load(p.residual + tok + e);
+    }
     __syncthreads();
 
     float ss = 0.f;
@@ -139,7 +172,9 @@ finalize_ar_kernel(const __grid_constant__ ArParams p) {
         float acc[VEC];
         if (active) {
             if (gather) {
-                const V sh = Ops::load(p.shared[r] + tok + e);
+                const V sh = (kHoist && q == 0)
+                                 ? sh_first
+                                 : Ops::load(static_cast<const uint16_t *>(dense_r) + tok + e);
                 const uint16_t *const *rows = s_row + r * K;
                 const float *ws = s_w + r * K;
 #pragma unroll
@@ -164,8 +199,11 @@ finalize_ar_kernel(const __grid_constant__ ArParams p) {
                 Ops::to_f32(sh, f);
 #pragma unroll
                 for (int c = 0; c < VEC; ++c) acc[c] += f[c];
+            } else if (kHoist && q == 0) {
+#pragma unroll
+                for (int c = 0; c < VEC; ++c) acc[c] = part_first[c];
             } else {
-                FOps::load(p.partial[r] + tok + e, acc);
+                FOps::load(static_cast<const float *>(dense_r) + tok + e, acc);
             }
         }
         if (lanes > 1) {
@@ -253,8 +291,11 @@ finalize_ar_kernel(const __grid_constant__ ArParams p) {
 }
 
 template <int VEC, bool NORM, bool CLUSTER, int PASSES>
-cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream) {
-    auto kern = finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES>;
+cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms,
+                        cudaStream_t stream) {
+    const int small = plan.grid <= num_sms ? 1 : 0;
+    auto kern = small ? finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES, 1>
+                      : finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES, 2>;
     cudaLaunchAttribute attr[2];
     unsigned num_attrs = 0;
     attr[num_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -263,15 +304,16 @@ cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, cudaStream_
     if (CLUSTER) {
         if (plan.cluster > 8) {
             // clusters of 9..16 CTAs are opt-in per kernel and device
-            static std::atomic<int> enabled[64];
+            static std::atomic<int> enabled[2][64];
             int dev = 0;
             cudaError_t err = cudaGetDevice(&dev);
             if (err != cudaSuccess) return err;
             if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-            if (!enabled[dev].load(std::memory_order_relaxed)) {
+            std::atomic<int> &done = enabled[small][dev];
+            if (!done.load(std::memory_order_relaxed)) {
                 err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                 if (err != cudaSuccess) return err;
-                enabled[dev].store(1, std::memory_order_relaxed);
+                done.store(1, std::memory_order_relaxed);
             }
         }
         attr[num_attrs].id = cudaLaunchAttributeClusterDimension;
@@ -291,26 +333,29 @@ cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, cudaStream_
 }
 
 template <int VEC, bool CLUSTER>
-cudaError_t launch_ar_norm(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream) {
+cudaError_t launch_ar_norm(const ArParams &p, const moef_ar_plan &plan, int num_sms,
+                           cudaStream_t stream) {
     switch (plan.passes) {
-        case 1: return launch_ar_t<VEC, true, CLUSTER, 1>(p, plan, stream);
-        case 2: return launch_ar_t<VEC, true, CLUSTER, 2>(p, plan, stream);
-        case 4: return launch_ar_t<VEC, true, CLUSTER, 4>(p, plan, stream);
-        case 8: return launch_ar_t<VEC, true, CLUSTER, 8>(p, plan, stream);
+        case 1: return launch_ar_t<VEC, true, CLUSTER, 1>(p, plan, num_sms, stream);
+        case 2: return launch_ar_t<VEC, true, CLUSTER, 2>(p, plan, num_sms, stream);
+        case 4: return launch_ar_t<VEC, true, CLUSTER, 4>(p, plan, num_sms, stream);
+        case 8: return launch_ar_t<VEC, true, CLUSTER, 8>(p, plan, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 template <int VEC>
-cudaError_t launch_ar_vec(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream) {
-    if (!p.residual) return launch_ar_t<VEC, false, false, 0>(p, plan, stream);
-    if (plan.cluster > 1) return launch_ar_norm<VEC, true>(p, plan, stream);
-    return launch_ar_norm<VEC, false>(p, plan, stream);
+cudaError_t launch_ar_vec(const ArParams &p, const moef_ar_plan &plan, int num_sms,
+                          cudaStream_t stream) {
+    if (!p.residual) return launch_ar_t<VEC, false, false, 0>(p, plan, num_sms, stream);
+    if (plan.cluster > 1) return launch_ar_norm<VEC, true>(p, plan, num_sms, stream);
+    return launch_ar_norm<VEC, false>(p, plan, num_sms, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_finalize_ar(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream) {
+cudaError_t launch_finalize_ar(const ArParams &p, const moef_ar_plan &plan, int num_sms,
+                               cudaStream_t stream) {
     // the plan must match the parameters it is launched with: one group of
     // nvc threads per lane, and with RMSNorm every vector of the slice
     // covered within the kernel's fixed number of passes
@@ -320,8 +365,8 @@ cudaError_t launch_finalize_ar(const ArParams &p, const moef_ar_plan &plan, cuda
     if (p.residual && static_cast<int64_t>(plan.passes) * plan.nvc < plan.slice)
         return cudaErrorInvalidValue;
     if (p.reduce == 0 && p.lanes * p.K > kMaxSlots) return cudaErrorInvalidValue;
-    if (plan.vec == 8) return launch_ar_vec<8>(p, plan, stream);
-    if (plan.vec == 1) return launch_ar_vec<1>(p, plan, stream);
+    if (plan.vec == 8) return launch_ar_vec<8>(p, plan, num_sms, stream);
+    if (plan.vec == 1) return launch_ar_vec<1>(p, plan, num_sms, stream);
     return cudaErrorInvalidValue;
 }
 

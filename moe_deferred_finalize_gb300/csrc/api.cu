@@ -231,6 +231,7 @@ moef_status check_finalize_args(const void *permuted_out, int64_t P, const int32
     p->K = K;
     p->H = H;
     p->routing_ready = 0;
+    p->pdl = 1;
     return MOEF_OK;
 }
 
@@ -249,7 +250,7 @@ moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *
                             int T, int K, int H, int splits_hint, int threads_hint,
                             unsigned flags, cudaStream_t stream) {
     if (splits_hint < 0 || threads_hint < 0) return MOEF_ERR_ARG;
-    if (flags & ~MOEF_FLAG_ROUTING_READY) return MOEF_ERR_ARG;
+    if (flags & ~(MOEF_FLAG_ROUTING_READY | MOEF_FLAG_NO_PDL)) return MOEF_ERR_ARG;
     moef::FinalizeParams p;
     bool vec_ok = false;
     moef_status st = check_finalize_args(permuted_out, P, idx_map, weights, wkind, routed_scale,
@@ -266,6 +267,7 @@ moef_status moe_finalize_ex(const void *permuted_out, int64_t P, const int32_t *
     if (st != MOEF_OK) return st;
     apply_plan(plan, &p);
     p.routing_ready = (flags & MOEF_FLAG_ROUTING_READY) ? 1 : 0;
+    p.pdl = (flags & MOEF_FLAG_NO_PDL) ? 0 : 1;
     return cuda_status(moef::launch_finalize(p, plan, sms, stream));
 }
 
@@ -516,7 +518,7 @@ moef_status launch_ar(moef::ArParams &p, int R, int T, int H, bool norm, bool ve
     p.nvc = plan.nvc;
     p.splits = plan.splits;
     p.slice = plan.slice;
-    return cuda_status(moef::launch_finalize_ar(p, plan, stream));
+    return cuda_status(moef::launch_finalize_ar(p, plan, sms, stream));
 }
 
 }  // namespace

@@ -241,9 +241,11 @@ cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, int num_sms
                         : finalize_kernel<VPT, VEC, NORM, CLUSTER, 0>;
     cudaLaunchAttribute attr[2];
     unsigned num_attrs = 0;
-    attr[num_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[num_attrs].val.programmaticStreamSerializationAllowed = 1;
-    ++num_attrs;
+    if (p.pdl) {
+        attr[num_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[num_attrs].val.programmaticStreamSerializationAllowed = 1;
+        ++num_attrs;
+    }
     if (CLUSTER) {
         if (plan.cluster > 8) {
             // Clusters of 9..16 CTAs are opt-in per kernel and device (setting

@@ -29,6 +29,7 @@ struct FinalizeParams {
     int splits;                 // CTAs per token
     int slice;                  // vectors per CTA
     int routing_ready;          // idx/weights may be read before the grid dependency wait
+    int pdl;                    // launched as a programmatic dependent of the previous kernel
 };
 
 // Launches one finalize according to `plan` (validated by the caller) on a
@@ -62,8 +63,10 @@ struct ArParams {
     int reduce;                                 // 1: sum fp32 partials (phase 2)
 };
 
-// Launches the all-reduce-fused finalize kernel according to `plan`.
-cudaError_t launch_finalize_ar(const ArParams &p, const moef_ar_plan &plan, cudaStream_t stream);
+// Launches the all-reduce-fused finalize kernel according to `plan` on a
+// device with `num_sms` multiprocessors.
+cudaError_t launch_finalize_ar(const ArParams &p, const moef_ar_plan &plan, int num_sms,
+                               cudaStream_t stream);
 
 // Launches the unfused three-kernel finalize (combine into tmp, add the
 // shared output, residual + RMSNorm); `plan` is a plan without RMSNorm.

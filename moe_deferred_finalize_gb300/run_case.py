@@ -6,6 +6,7 @@ For profilers: one process, a handful of launches, a known input size.
   python -m moe_deferred_finalize_gb300.run_case --prefill-tokens 4096 --iters 3
   python -m moe_deferred_finalize_gb300.run_case --workload decode_bs1_packed --unfused
   python -m moe_deferred_finalize_gb300.run_case --gate-tokens 16384 --iters 3
+  python -m moe_deferred_finalize_gb300.run_case --tp 8 16 --form one_shot --iters 3
 """
 import argparse
 
@@ -30,6 +31,12 @@ def main(argv=None):
     g.add_argument("--prefill-tokens", type=int)
     g.add_argument("--gate-tokens", type=int,
                    help="run the top-K gate (E=256, K=8, sigmoid, packed) on this many tokens")
+    g.add_argument("--tp", type=int, nargs=2, metavar=("R", "T"),
+                   help="the all-reduce-fused finalize over R ranks at decode batch T "
+                        "(1, 16 or 256), H=7168, residual + RMSNorm")
+    ap.add_argument("--form", choices=["one_shot", "two_phase", "plain"], default="one_shot",
+                    help="with --tp: one-shot, two-phase (phase 1 per rank, then phase 2), "
+                         "or the plain finalize of rank 0's operands")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--write-out", action="store_true",
                     help="with a residual, also write out (default: residual_out + norm_out only)")
@@ -44,6 +51,27 @@ def main(argv=None):
             mf.topk_route(z, 8, "sigmoid", want_packed=True)
         torch.cuda.synchronize()
         print(f"gate: T={args.gate_tokens} E=256 K=8 iters={args.iters} ok")
+        return
+    if args.tp:
+        R, T = args.tp
+        g = W.tp_decode(R, T)
+        ranks = [{"permuted_out": _dev(wl.permuted_out), "idx_map": _dev(wl.idx),
+                  "weights": _dev(wl.weights), "shared_out": _dev(wl.shared)} for wl in g.ranks]
+        ep = dict(residual=_dev(g.residual), gamma=_dev(g.gamma), eps=g.eps, write_out=False)
+        for _ in range(args.iters):
+            if args.form == "one_shot":
+                mf.moe_finalize_allreduce(ranks, g.wkind, routed_scale=g.routed_scale, **ep)
+            elif args.form == "two_phase":
+                parts = [mf.moe_finalize_partial(r["permuted_out"], r["idx_map"], r["weights"],
+                                                 g.wkind, r["shared_out"],
+                                                 routed_scale=g.routed_scale) for r in ranks]
+                mf.moe_finalize_allreduce_reduce(parts, **ep)
+            else:
+                r0 = ranks[0]
+                mf.moe_finalize(r0["permuted_out"], r0["idx_map"], r0["weights"], g.wkind,
+                                r0["shared_out"], routed_scale=g.routed_scale, **ep)
+        torch.cuda.synchronize()
+        print(f"tp: R={R} T={T} form={args.form} iters={args.iters} ok")
         return
     wl = W.make(args.workload) if args.workload else W.prefill(args.prefill_tokens)
     x, idx, w, sh = _dev(wl.permuted_out), _dev(wl.idx), _dev(wl.weights), _dev(wl.shared)

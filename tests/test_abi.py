@@ -59,8 +59,10 @@ def test_library_of_another_interface_version_is_refused(mf, monkeypatch):
 
 def test_unknown_flags_rejected(mf):
     f = mf.lib().moe_finalize_ex
-    assert f(A, 16, A, A, 0, 1.0, A, None, None, 1e-6, A, None, None, 0, 2, 8, 0, 0, 2, None) == 4
-    assert f(A, 16, A, A, 0, 1.0, A, None, None, 1e-6, A, None, None, 0, 2, 8, 0, 0, 1, None) == 0
+    assert f(A, 16, A, A, 0, 1.0, A, None, None, 1e-6, A, None, None, 0, 2, 8, 0, 0, 4, None) == 4
+    for flags in (1, 2, 3):     # MOEF_FLAG_ROUTING_READY, MOEF_FLAG_NO_PDL
+        assert f(A, 16, A, A, 0, 1.0, A, None, None, 1e-6, A, None, None, 0, 2, 8, 0, 0, flags,
+                 None) == 0
 
 
 def test_status_strings(mf):
@@ -386,7 +388,7 @@ def test_fastcall_packs_arguments_in_abi_order(mf):
              dict(out=None), dict(residual=A), dict(gamma=A), dict(residual_out=A),
              dict(norm_out=A), dict(wkind=3), dict(K=33), dict(H=0), dict(P=0), dict(x=A + 1),
              dict(out=A + 1), dict(idx=A + 2), dict(w=A + 2), dict(splits=-1),
-             dict(flags=2), dict(residual=A, gamma=A, residual_out=A, norm_out=A, eps=-1.0)]
+             dict(flags=4), dict(residual=A, gamma=A, residual_out=A, norm_out=A, eps=-1.0)]
     seen = set()
     for c in cases:
         a = {**base, **c}

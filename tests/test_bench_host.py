@@ -88,3 +88,30 @@ def test_cpu_baselines_time_the_oracle_on_every_token():
     assert threads == len(os.sched_getaffinity(0))
     assert bench.writes_out("fused_norm_bs16", wl)
     assert not bench.writes_out(bench.WORKLOAD, W.Workload(**{**wl.__dict__, "name": bench.WORKLOAD}))
+
+
+def test_allreduce_bytes():
+    # R ranks' rows, shared output and fp32 routing, then residual in and
+    # residual_out + norm_out written, gamma once
+    T, K, H = 16, 8, 7168
+    for R in (1, 2, 8):
+        want = R * (T * K * H * 2 + T * H * 2 + T * K * 8) + 3 * T * H * 2 + H * 2
+        assert bench.allreduce_bytes(R, T, K, H) == want
+    # one rank with residual + RMSNorm and no out is the plain finalize's count
+    assert bench.allreduce_bytes(1, T, K, H) == bench.algorithmic_bytes(T, K, H, 4, True, False)
+
+
+def test_per_config_summary_puts_the_oracle_beside_each_workload():
+    decode = {k: {"us_per_call_graph": 2.0, "GBps_graph": 100.0, "frac": 0.01,
+                  "us_bytes_at_peak": 0.1, "floor_us_dependent_launch": 1.7}
+              for k in bench.CONFIG_KEYS.values()}
+    cpu = {"workloads_ms": {n: {"one_thread": 1.0, "all_cores": 0.5}
+                            for n in list(bench.CONFIG_KEYS) + [bench.WORKLOAD]}}
+    out = bench.per_config_summary(decode, 0.4, 7000.0, 7000.0, 2_819_635_200, cpu)
+    assert set(out) == set(bench.CONFIG_KEYS) | {bench.WORKLOAD}
+    for v in out.values():
+        assert {"us_per_call", "GBps", "frac", "oracle_ms_one_thread",
+                "oracle_ms_all_cores"} <= set(v)
+    assert out[bench.WORKLOAD]["frac"] == 1.0 and out[bench.WORKLOAD]["us_per_call"] == 400.0
+    # without a CPU leg the GPU figures stand alone
+    assert "oracle_ms_one_thread" not in bench.per_config_summary(decode, 0.4, 1, 1, 1, None)["tiny"]

@@ -164,9 +164,12 @@ def test_routing_ready_flag_same_result(cuda_lib, name):
     dev = to_device(wl)
     a = run_gpu(cuda_lib, wl, dev)
     b = run_gpu(cuda_lib, wl, dev, routing_ready=True)
+    c = run_gpu(cuda_lib, wl, dev, pdl=False)             # MOEF_FLAG_NO_PDL
+    d = run_gpu(cuda_lib, wl, dev, routing_ready=True, pdl=False)
     for key in a:
         if a[key] is not None:
-            assert np.array_equal(bits_of(a[key]), bits_of(b[key])), key
+            for other in (b, c, d):
+                assert np.array_equal(bits_of(a[key]), bits_of(other[key])), key
 
 
 def test_one_slot_weight_one_is_the_row(cuda_lib):

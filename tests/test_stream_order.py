@@ -72,8 +72,12 @@ def test_routing_ready_with_producer_of_rows(cuda_lib):
     src = dev["x"].clone()
     dev["x"].zero_()
     torch.cuda.synchronize()
-    torch.mul(src, 1.0, out=dev["x"])                           # producer of the rows
-    out = cuda_lib.moe_finalize(dev["x"], dev["idx"], dev["w"], "fp32", dev["shared"],
-                                routed_scale=wl.routed_scale, routing_ready=True)["out"]
-    torch.cuda.synchronize()
-    assert np.array_equal(bits_of(out), bits_of(base))
+    for pdl in (True, False):
+        dev["x"].zero_()
+        torch.cuda.synchronize()
+        torch.mul(src, 1.0, out=dev["x"])                       # producer of the rows
+        out = cuda_lib.moe_finalize(dev["x"], dev["idx"], dev["w"], "fp32", dev["shared"],
+                                    routed_scale=wl.routed_scale, routing_ready=True,
+                                    pdl=pdl)["out"]
+        torch.cuda.synchronize()
+        assert np.array_equal(bits_of(out), bits_of(base)), pdl
