@@ -393,9 +393,14 @@ int pow2_bucket(int need) {
 //  * without RMSNorm, 128 threads per CTA (R groups of 128 / R, at least 16
 //    threads), one vector per thread: slices of 128 / R vectors;
 //  * with RMSNorm, one CTA or one cluster of up to 16 CTAs finishes a row.
-//    Groups of up to 512 / R threads (at most 256), a multiple of 32: with
-//    R = 8 at H = 7168, 14 CTAs of 8 x 64 threads.  The split is halved while
-//    the grid exceeds 4 CTAs per SM, each thread then taking up to 8 passes.
+//    Each extra pass over a slice costs a full chain of loads, barrier and
+//    epilogue (about 2.8 us at R = 8, T = 1), so a few tokens take CTAs of
+//    up to 512 threads (R groups of 512 / R, at most 256), enough for one
+//    pass: with R = 8 at H = 7168, 14 CTAs of 8 x 64 threads.  From T = 5 on
+//    CTAs of 256 threads win even with a second pass (R = 4, T = 16: 14 x
+//    256 threads 5.6 us vs 7 x 512 threads 9.3 us; R = 8: 16 x 224 threads
+//    9.2 us vs 14 x 512 threads 11.9 us).  The split is halved while the grid
+//    exceeds 4 CTAs per SM, each thread then taking up to 8 passes.
 moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int vec_ok,
                                         int num_sms, moef_ar_plan *plan) {
     if (!plan) return MOEF_ERR_NULL;
@@ -418,7 +423,7 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
         }
         passes = ceil_div(slice, nvc);
     } else {
-        int nvc_max = kArMaxThreads / R;
+        int nvc_max = (T <= 4 ? kArMaxThreads : kArMaxThreads / 2) / R;
         if (nvc_max > 256) nvc_max = 256;
         nvc_max = nvc_max / 32 * 32;
         splits = ceil_div(nvec, nvc_max);

@@ -308,6 +308,50 @@ def test_allreduce_plans(mf):
         mf.allreduce_plan(9, 1, 7168, True)
 
 
+def test_allreduce_kernel_indices_stay_in_their_buffers(mf):
+    """The all-reduce kernel's index arithmetic, replayed on the host for
+    every plan of the decode, test and benchmark shapes: each thread's rank
+    and vector, the shared-memory words it writes (the ranks' partials of a
+    pass, the kept residual_out vectors), the slot staging and the cluster
+    pushes all stay inside what the plan allocates."""
+    for R in range(1, 9):
+        for T in (1, 4, 5, 16, 256, 1024):
+            for H in (64, 100, 512, 1000, 2048, 4096, 4104, 5120, 7168, 16384):
+                for norm in (False, True):
+                    try:
+                        p = mf.allreduce_plan(R, T, H, norm)
+                    except mf.MoefError:
+                        continue
+                    vec, nvc, lanes, threads = p["vec"], p["nvc"], p["lanes"], p["threads"]
+                    nvec = H // vec
+                    vbytes = 16 if vec == 8 else 2
+                    sp_bytes = 4 * vec * lanes * nvc if lanes > 1 else 0
+                    keep_bytes = p["passes"] * nvc * vbytes if norm else 0
+                    assert sp_bytes + keep_bytes == p["smem_bytes"]
+                    assert threads <= 512 and threads // 32 <= 16 and R * 32 <= 256
+                    for split in range(p["splits"]):
+                        v_begin = split * p["slice"]
+                        v_end = min(v_begin + p["slice"], nvec)
+                        for tid in range(threads):
+                            r, j = divmod(tid, nvc)
+                            assert r < lanes
+                            # partial word (r, j, c) of a pass
+                            assert (r * nvc + j + 1) * vec * 4 <= max(sp_bytes, 4 * vec * nvc)
+                            q = 0
+                            for base in range(v_begin, v_end, nvc):
+                                v = base + j
+                                if v < v_end:
+                                    assert v * vec + vec <= H
+                                    if norm:
+                                        assert sp_bytes + (q * nvc + j + 1) * vbytes <= \
+                                            p["smem_bytes"]
+                                q += 1
+                            if norm:
+                                assert q <= p["passes"]
+                    if norm and p["cluster"] > 1:
+                        assert p["cluster"] == p["splits"] <= min(16, threads)
+
+
 def test_every_accepted_norm_plan_covers_its_slice_in_one_pass(mf):
     """The RMSNorm kernel makes one pass over its slice, and its launcher
     refuses a plan that leaves vectors without a thread; so every plan the

@@ -273,13 +273,13 @@ def test_graph_capture_replay(cuda_lib, orc):
 
 @pytest.mark.slow
 def test_large_t_sampled_rows(cuda_lib, orc):
-    """T = 1024 with R = 8 at H = 4096 (one CTA per row, 8 passes per
+    """T = 1024 with R = 8 at H = 4096 (2-CTA clusters, 8 passes per
     thread): sampled token rows against the oracle, every row against the
     two-phase form."""
     g = W.tp_group("large", 8, T=1024, K=8, H=4096, E=512, tile=64, P=16384,
                    routed_scale=2.5, seed=9)
     p = cuda_lib.allreduce_plan(8, 1024, 4096, True)
-    assert (p["splits"], p["passes"]) == (1, 8)
+    assert (p["splits"], p["passes"]) == (2, 8)
     rd = ranks_dev(g)
     a = one_shot(cuda_lib, g, rd)
     b, _ = two_phase(cuda_lib, g, rd)
