@@ -315,7 +315,7 @@ def time_roofline(mf, wl, d, outs, device, min_seconds):
     return [a.elapsed_time(b) for a, b in ev], (t0, t1)
 
 
-def decode_latency(mf, name, device, reps, peak, producer=False):
+def decode_latency(mf, name, device, reps, peak, producer=False, sequential=False):
     """µs per call on inputs rotated through copies whose total exceeds L2.
 
     With ``producer``: also the µs the finalize adds behind a kernel that
@@ -323,7 +323,11 @@ def decode_latency(mf, name, device, reps, peak, producer=False):
     written permuted_out: (producer + finalize) - (producer alone) per call,
     both as CUDA-graph replays, with the finalize launched as a programmatic
     dependent (the default), as a plain stream-ordered kernel, and with
-    MOEF_FLAG_ROUTING_READY."""
+    MOEF_FLAG_ROUTING_READY.
+
+    With ``sequential``: also the same calls with a row map that reads
+    consecutive rows (t * K + k) instead of each token's expert rows, which
+    isolates what the gather itself costs."""
     wl = W.make(name)
     d = device_inputs(wl, device)
     norm = wl.with_norm
@@ -412,6 +416,17 @@ def decode_latency(mf, name, device, reps, peak, producer=False):
            "copies": R, "calls": n_pass * R,
            "plan": mf.plan(wl.T, wl.K, wl.H, norm, True,
                            torch.cuda.get_device_properties(device).multi_processor_count)}
+
+    if sequential:
+        seq = torch.arange(wl.T * wl.K, dtype=torch.int32, device=device).view(wl.T, wl.K)
+        assert wl.T * wl.K <= wl.P
+
+        def one_pass_seq():
+            for dd, oo in sets:
+                call(mf, wl, {**dd, "idx": seq}, oo)
+
+        res["us_per_call_graph_sequential_rows"] = round(graph(one_pass_seq), 3)
+        del seq
 
     if producer:
         # Two producers rewrite each copy's row buffer [P, H] just before its
@@ -876,7 +891,8 @@ def run_ours(args, ws, rank, local):
     if not args.skip_decode:
         decode = {"T1": decode_latency(mf, "decode_bs1_packed", device, 4000, peak,
                                        producer=True),
-                  "T256": decode_latency(mf, "decode_bs256", device, 2000, peak, producer=True),
+                  "T256": decode_latency(mf, "decode_bs256", device, 2000, peak, producer=True,
+                                         sequential=True),
                   "T16_rmsnorm": decode_latency(mf, "fused_norm_bs16", device, 2000, peak,
                                                 producer=True),
                   "T4_tiny": decode_latency(mf, "tiny", device, 2000, peak)}

@@ -13,6 +13,7 @@ import os
 from typing import Optional
 
 import torch
+import torch.utils.dlpack
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_finalize.so")
 ABI_VERSION = 1     # MOEF_ABI_VERSION of include/moe_finalize.h
@@ -292,6 +293,12 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
     kernel on the stream started (MOEF_FLAG_ROUTING_READY).  ``pdl=False``:
     launch as a plain stream-ordered kernel (MOEF_FLAG_NO_PDL).
     """
+    res = _checked_fast(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
+                        residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
+                        threads, (FLAG_ROUTING_READY if routing_ready else 0) |
+                        (0 if pdl else FLAG_NO_PDL), stream)
+    if res is not None:
+        return res
     args, res = _marshal(permuted_out, idx_map, weights, wkind, shared_out, routed_scale,
                          residual, gamma, eps, out, residual_out, norm_out, write_out, splits,
                          threads, routing_ready=routing_ready, pdl=pdl)
@@ -300,6 +307,64 @@ def moe_finalize(permuted_out: torch.Tensor, idx_map: torch.Tensor, weights: tor
         st = _call_ex(args, _stream(stream, device))
     if st != 0:
         raise MoefError(st, "moe_finalize")
+    return res
+
+
+# DLPack element types of the weight encodings (code, bits): fp32, bf16 bits,
+# packed int32 words
+_WCODE = {"fp32": (2, 32), "bf16": (4, 16), "packed": (0, 32)}
+_TO_DLPACK = torch.utils.dlpack.to_dlpack
+
+
+def _checked_fast(permuted_out, idx_map, weights, wkind, shared_out, routed_scale, residual,
+                  gamma, eps, out, residual_out, norm_out, write_out, splits, threads, flags,
+                  stream):
+    """The checked call in one pass through the _fastcall extension: each
+    tensor is described by one DLPack export, and the extension checks
+    device, dtype, rank, shapes and layout before calling moe_finalize_ex.
+    Returns the result dict, or None when the extension is missing or any
+    check fails (the caller then runs the Python checks, which name the
+    problem); a failed library status raises as usual."""
+    fast = _fastcall()
+    if fast is None or wkind not in _WCODE or not isinstance(shared_out, torch.Tensor):
+        return None
+    try:
+        dev = permuted_out.get_device()
+        if dev < 0 or dev != torch.cuda.current_device():
+            return None
+        if residual is not None:
+            if residual_out is None:
+                residual_out = torch.empty_like(shared_out)
+            if norm_out is None:
+                norm_out = torch.empty_like(shared_out)
+            if not write_out:
+                out = None
+            elif out is None:
+                out = torch.empty_like(shared_out)
+        elif out is None:
+            out = torch.empty_like(shared_out)
+        d = _TO_DLPACK
+        caps = [None if t is None else d(t)
+                for t in (permuted_out, idx_map, weights, shared_out, residual, gamma, out,
+                          residual_out, norm_out)]
+    except (AttributeError, TypeError, RuntimeError):
+        return None
+    global _EX_ADDRESS
+    if _EX_ADDRESS is None:
+        _EX_ADDRESS = ctypes.cast(_lib().moe_finalize_ex, ctypes.c_void_p).value
+    code, bits = _WCODE[wkind]
+    st = fast.checked_call(_EX_ADDRESS, WKIND[wkind], code, bits, float(routed_scale),
+                           float(eps), dev, int(splits), int(threads), flags,
+                           _RAW_STREAM(dev) if stream is None and _RAW_STREAM is not None
+                           else _stream(stream, torch.device("cuda", dev)), *caps)
+    if st < 0:
+        return None
+    if st != 0:
+        raise MoefError(st, "moe_finalize")
+    res = {"out": out}
+    if residual is not None:
+        res["residual_out"] = residual_out
+        res["norm_out"] = norm_out
     return res
 
 

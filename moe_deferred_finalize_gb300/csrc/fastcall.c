@@ -5,8 +5,9 @@
  * host time than the decode-size kernel takes on the GPU.  Here call_now
  * converts them directly, and pack/call go further for repeated calls: the
  * arguments are packed once into a C struct (a capsule) and each call passes
- * only the stream.  It does no computation and no checking beyond what the
- * C ABI itself does.
+ * only the stream.  checked_call does the Python binding's argument checks
+ * on DLPack descriptions of the tensors before calling.  Nothing here
+ * computes anything of the finalize.
  */
 #define PY_SSIZE_T_CLEAN
 #include <Python.h>
@@ -116,6 +117,133 @@ static PyObject *call_now(PyObject *self, PyObject *const *args, Py_ssize_t narg
     return PyLong_FromLong(enqueue(&b, stream));
 }
 
+/* ---------------------------------------------------------------------------
+ * checked_call: the checks of the Python binding, done here on DLPack
+ * descriptions of the tensors (one capsule per tensor, as torch's
+ * to_dlpack() makes them), then one moe_finalize_ex call.  Reading a
+ * tensor's device, dtype, shape, strides and address costs one DLPack
+ * export instead of six attribute lookups.
+ *
+ * The structures below are the DLPack interchange format (DLTensor inside a
+ * DLManagedTensor, capsule name "dltensor"): a public interface that any
+ * consumer has to lay out the same way.  The capsules are only read; each
+ * one's own destructor releases its tensor.
+ */
+typedef struct {
+    int32_t device_type;
+    int32_t device_id;
+} dl_device;
+
+typedef struct {
+    uint8_t code;
+    uint8_t bits;
+    uint16_t lanes;
+} dl_dtype;
+
+typedef struct {
+    void *data;
+    dl_device device;
+    int32_t ndim;
+    dl_dtype dtype;
+    int64_t *shape;
+    int64_t *strides;
+    uint64_t byte_offset;
+} dl_tensor;
+
+typedef struct {
+    dl_tensor t;
+    void *manager_ctx;
+    void (*deleter)(void *self);
+} dl_managed;
+
+enum { DL_INT = 0, DL_FLOAT = 2, DL_BFLOAT = 4 };
+enum { DL_CUDA = 2 };
+
+/* a tensor description; NULL for None (or on error, with a Python error) */
+static const dl_tensor *described(PyObject *cap) {
+    if (cap == Py_None) return NULL;
+    dl_managed *m = (dl_managed *)PyCapsule_GetPointer(cap, "dltensor");
+    return m ? &m->t : NULL;
+}
+
+/* 1 when t is a dense row-major array on CUDA device `dev` of element type
+ * (code, bits), with ndim dimensions; its sizes go to dims */
+static int dense(const dl_tensor *t, int dev, uint8_t code, uint8_t bits, int ndim,
+                 int64_t *dims) {
+    if (!t || t->device.device_type != DL_CUDA || t->device.device_id != dev) return 0;
+    if (t->dtype.code != code || t->dtype.bits != bits || t->dtype.lanes != 1) return 0;
+    if (t->ndim != ndim) return 0;
+    int64_t stride = 1;
+    for (int d = ndim - 1; d >= 0; --d) {
+        dims[d] = t->shape[d];
+        if (t->strides && t->shape[d] != 1 && t->strides[d] != stride) return 0;
+        stride *= t->shape[d];
+    }
+    return 1;
+}
+
+static void *address(const dl_tensor *t) {
+    return t ? (void *)((char *)t->data + t->byte_offset) : NULL;
+}
+
+/* checked_call(fn_address, wkind, weight_code, weight_bits, routed_scale,
+ *              eps, device, splits, threads, flags, stream, permuted_out,
+ *              idx_map, weights, shared_out, residual, gamma, out,
+ *              residual_out, norm_out) -> status
+ * The last nine are DLPack capsules or None.  Returns moe_finalize_ex's
+ * status, or -1 when a tensor fails the binding's checks (wrong device,
+ * dtype, rank, shape or layout, or a missing or extra tensor): the caller
+ * then runs its own checks to report which. */
+static PyObject *checked_call(PyObject *self, PyObject *const *a, Py_ssize_t nargs) {
+    (void)self;
+    if (nargs != 20) {
+        PyErr_SetString(PyExc_TypeError, "checked_call takes 20 arguments");
+        return NULL;
+    }
+    finalize_ex_fn fn = (finalize_ex_fn)as_ptr(a[0]);
+    const int wkind = (int)PyLong_AsLong(a[1]);
+    const uint8_t wcode = (uint8_t)PyLong_AsLong(a[2]);
+    const uint8_t wbits = (uint8_t)PyLong_AsLong(a[3]);
+    const float scale = (float)PyFloat_AsDouble(a[4]);
+    const float eps = (float)PyFloat_AsDouble(a[5]);
+    const int dev = (int)PyLong_AsLong(a[6]);
+    const int splits = (int)PyLong_AsLong(a[7]);
+    const int threads = (int)PyLong_AsLong(a[8]);
+    const unsigned flags = (unsigned)PyLong_AsUnsignedLong(a[9]);
+    void *stream = as_ptr(a[10]);
+    if (PyErr_Occurred()) return NULL;
+    if (!fn) {
+        PyErr_SetString(PyExc_ValueError, "null function pointer");
+        return NULL;
+    }
+    const dl_tensor *t[9];
+    for (int i = 0; i < 9; ++i) {
+        t[i] = described(a[11 + i]);
+        if (PyErr_Occurred()) return NULL;
+    }
+    const dl_tensor *x = t[0], *idx = t[1], *w = t[2], *sh = t[3], *res = t[4], *gam = t[5],
+                    *out = t[6], *rout = t[7], *nout = t[8];
+    int64_t xd[2], id[2], d2[2], d1[1];
+    int ok = dense(x, dev, DL_BFLOAT, 16, 2, xd) && dense(idx, dev, DL_INT, 32, 2, id) &&
+             dense(w, dev, wcode, wbits, 2, d2) && d2[0] == id[0] && d2[1] == id[1] &&
+             dense(sh, dev, DL_BFLOAT, 16, 2, d2) && d2[0] == id[0] && d2[1] == xd[1];
+    const int norm = res != NULL;
+    if (ok && (norm != (gam != NULL) || norm != (rout != NULL) || norm != (nout != NULL) ||
+               (!norm && !out)))
+        ok = 0;
+    const dl_tensor *rows[4] = {res, out, rout, nout};
+    for (int i = 0; ok && i < 4; ++i)
+        if (rows[i])
+            ok = dense(rows[i], dev, DL_BFLOAT, 16, 2, d2) && d2[0] == id[0] && d2[1] == xd[1];
+    if (ok && gam) ok = dense(gam, dev, DL_BFLOAT, 16, 1, d1) && d1[0] == xd[1];
+    if (ok && (xd[1] > 0x7FFFFFFF || id[0] > 0x7FFFFFFF || id[1] > 0x7FFFFFFF)) ok = 0;
+    if (!ok) return PyLong_FromLong(-1);
+    return PyLong_FromLong(fn(address(x), xd[0], (const int32_t *)address(idx), address(w),
+                              wkind, scale, address(sh), address(res), address(gam), eps,
+                              address(out), address(rout), address(nout), (int)id[0],
+                              (int)id[1], (int)xd[1], splits, threads, flags, stream));
+}
+
 /* call(capsule, stream_handle) -> status of moe_finalize_ex */
 static PyObject *call(PyObject *self, PyObject *const *args, Py_ssize_t nargs) {
     (void)self;
@@ -137,6 +265,8 @@ static PyMethodDef methods[] = {
      "Enqueue a packed call on a stream; returns the status."},
     {"call_now", (PyCFunction)(void (*)(void))call_now, METH_FASTCALL,
      "Enqueue one moe_finalize_ex call from its arguments; returns the status."},
+    {"checked_call", (PyCFunction)(void (*)(void))checked_call, METH_FASTCALL,
+     "Check DLPack-described tensors and enqueue one moe_finalize_ex call."},
     {NULL, NULL, 0, NULL},
 };
 

@@ -461,3 +461,73 @@ def test_calls_switch_to_the_tensors_device(monkeypatch):
     assert isinstance(_abi._on(torch.device("cuda")), contextlib.nullcontext)
     guard = _abi._on(torch.device("cuda", 1))
     assert isinstance(guard, torch.cuda.device) and guard.idx == 1
+
+
+def test_fastcall_checked_call_refuses_what_the_binding_refuses(mf):
+    """checked_call does the binding's checks on DLPack descriptions: one
+    hand-made description per tensor (made-up addresses, never read), each
+    single violation refused with -1; a valid set passes the checks and
+    reaches the library, which returns its CUDA status here (no GPU)."""
+    from moe_deferred_finalize_gb300 import _abi
+    fast = _abi._fastcall()
+    if fast is None:
+        pytest.skip("_fastcall not built (no Python headers)")
+
+    class DLTensor(ctypes.Structure):
+        _fields_ = [("data", ctypes.c_void_p), ("device_type", ctypes.c_int32),
+                    ("device_id", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                    ("code", ctypes.c_uint8), ("bits", ctypes.c_uint8),
+                    ("lanes", ctypes.c_uint16), ("shape", ctypes.POINTER(ctypes.c_int64)),
+                    ("strides", ctypes.POINTER(ctypes.c_int64)),
+                    ("byte_offset", ctypes.c_uint64)]
+
+    class DLManaged(ctypes.Structure):
+        _fields_ = [("t", DLTensor), ("ctx", ctypes.c_void_p), ("deleter", ctypes.c_void_p)]
+
+    new_capsule = ctypes.pythonapi.PyCapsule_New
+    new_capsule.restype = ctypes.py_object
+    new_capsule.argtypes = [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_void_p]
+    keep = []
+
+    def cap(shape, code=4, bits=16, dev=0, dev_type=2, strides=None, addr=A):
+        shp = (ctypes.c_int64 * len(shape))(*shape)
+        st = None
+        if strides is not None:
+            st = (ctypes.c_int64 * len(strides))(*strides)
+        m = DLManaged(DLTensor(addr, dev_type, dev, len(shape), code, bits, 1,
+                               ctypes.cast(shp, ctypes.POINTER(ctypes.c_int64)),
+                               ctypes.cast(st, ctypes.POINTER(ctypes.c_int64)) if st else None,
+                               0), None, None)
+        keep.extend([shp, st, m])
+        return new_capsule(ctypes.addressof(m), b"dltensor", None)
+
+    T, K, H, P = 3, 2, 16, 8
+    fn = ctypes.cast(mf.lib().moe_finalize_ex, ctypes.c_void_p).value
+
+    def base():
+        return dict(x=cap((P, H)), idx=cap((T, K), 0, 32), w=cap((T, K), 2, 32),
+                    sh=cap((T, H)), res=None, gam=None, out=cap((T, H)), rout=None, nout=None)
+
+    def run(**kw):
+        a = {**base(), **kw}
+        return fast.checked_call(fn, 0, 2, 32, 1.0, 1e-6, 0, 0, 0, 0, 0,
+                                 a["x"], a["idx"], a["w"], a["sh"], a["res"], a["gam"],
+                                 a["out"], a["rout"], a["nout"])
+
+    passes = run()
+    assert passes in (0, 5)       # the library ran: launched, or no CUDA device here
+    norm = dict(res=cap((T, H)), gam=cap((H,)), rout=cap((T, H)), nout=cap((T, H)))
+    assert run(**norm) == passes and run(**{**norm, "out": None}) == passes
+    bad = [dict(x=cap((P, H), dev=1)), dict(x=cap((P, H), dev_type=1)),
+           dict(x=cap((P, H), code=2, bits=32)), dict(x=cap((P, H, 1))),
+           dict(x=cap((P, H), strides=(1, P))), dict(idx=cap((T, K), 2, 32)),
+           dict(idx=cap((T + 1, K), 0, 32)), dict(w=cap((T, K), 4, 16)),
+           dict(w=cap((T, K + 1), 2, 32)), dict(sh=cap((T, H + 8))), dict(sh=cap((T + 1, H))),
+           dict(out=None), dict(out=cap((T, H), code=0)), dict(out=cap((T, H), strides=(H + 8, 1))),
+           dict(res=cap((T, H))), dict(rout=cap((T, H))), dict(**{**norm, "nout": None}),
+           dict(**{**norm, "gam": cap((H + 8,))}), dict(**{**norm, "rout": cap((T, H - 8))})]
+    for kw in bad:
+        assert run(**kw) == -1, kw
+    # a strided size-1 dimension is still dense (torch reports such strides)
+    assert run(out=cap((1, H), strides=(999, 1)), sh=cap((1, H)), idx=cap((1, K), 0, 32),
+               w=cap((1, K), 2, 32)) == passes
