@@ -292,3 +292,40 @@ def test_large_t_sampled_rows(cuda_lib, orc):
     ref = oracle_ar(orc, sub)
     for key in ref:
         assert_close(f64_of(a[key])[rows], ref[key], f"T=1024 sampled {key}")
+
+
+def test_tp_orchestration_one_rank(cuda_lib, orc):
+    """The tensor-parallel orchestration with its CUDA transport (IPC
+    handles, interprocess events) and library backend, as one rank of a
+    one-rank gloo group: two steps of different token counts, through both
+    partial buffers, against the oracle."""
+    import socket
+    import torch.distributed as dist
+    from moe_deferred_finalize_gb300 import tp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                           world_size=1)
+    try:
+        group = tp.TPFinalize(dist.group.WORLD, 16, 7168)
+        for T in (16, 5):
+            g = W.tp_decode(1, 16, seed=T)
+            if T != 16:
+                wl = g.ranks[0]
+                g = W.TPGroup("sub", [W.Workload(**{**wl.__dict__, "T": T, "idx": wl.idx[:T],
+                                                    "weights": wl.weights[:T],
+                                                    "shared": wl.shared[:T]})],
+                              g.residual[:T], g.gamma, g.eps)
+            rd = ranks_dev(g)[0]
+            ep = epilogue_dev(g)
+            outs = {k: torch.empty((T, 7168), dtype=torch.bfloat16, device="cuda")
+                    for k in ("out", "residual_out", "norm_out")}
+            res = group.step(rd, g.wkind, g.routed_scale, T, residual=ep["residual"],
+                             gamma=ep["gamma"], eps=ep["eps"], outs=outs)
+            torch.cuda.synchronize()
+            compare(res, oracle_ar(orc, g), f"orchestrated T={T}: ")
+        assert group.step_index == 2
+        group.close()
+    finally:
+        dist.destroy_process_group()
