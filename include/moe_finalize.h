@@ -259,12 +259,11 @@ moef_status moe_finalize_unfused(const void *permuted_out, int64_t P,
 
 /*
  * moe_finalize_unfused_noalloc -- moe_finalize_unfused without a workspace
- * argument, for callers that cannot allocate device memory: code running
- * while a CUDA graph is being captured (cudaMalloc is not allowed there),
- * serving engines that fix every device allocation before they start and
- * forbid allocation on the request path, and plugins whose host framework
- * owns all device memory and gives them no allocator.  The pages have no
- * counterpart to this entry point.
+ * argument, for callers that cannot allocate device memory: serving engines
+ * that fix every device allocation before they start and forbid allocation
+ * on the request path, and plugins whose host framework owns all device
+ * memory and gives them no allocator.  The pages have no counterpart to this
+ * entry point.
  *
  * The workspace is a fixed array of MOEF_NOALLOC_SCRATCH_BYTES (8 MiB)
  * compiled into the library; every GPU on which the library's device code
@@ -275,7 +274,9 @@ moef_status moe_finalize_unfused(const void *permuted_out, int64_t P,
  *
  * Set-up: the first call made on a device looks up the array's device
  * address (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.
+ * call before any stream capture.  The address is kept for the life of the
+ * device's primary context: after cudaDeviceReset (or anything else that
+ * destroys that context) it is stale, and calls are not supported.
  *
  * Sharing: all calls on a device use the same array, and it keeps whatever
  * the last call left in it.  Nothing in it needs to start at zero (the first

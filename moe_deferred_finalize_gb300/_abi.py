@@ -413,8 +413,8 @@ def moe_finalize_unfused_noalloc(permuted_out: torch.Tensor, idx_map: torch.Tens
                                  out: torch.Tensor, residual_out: Optional[torch.Tensor] = None,
                                  norm_out: Optional[torch.Tensor] = None, stream=None) -> dict:
     """``moe_finalize_unfused`` for callers that cannot allocate device
-    memory (inside graph capture, fixed-memory serving engines, plugins with
-    no allocator): the workspace is the library's fixed 8 MiB scratch array,
+    memory (fixed-memory serving engines, plugins with no allocator): the
+    workspace is the library's fixed 8 MiB scratch array,
     so T * H * 2 must not exceed ``NOALLOC_SCRATCH_BYTES``.  All outputs must
     be given (this wrapper allocates nothing either).  Calls on one device
     share the scratch: order them (one stream, or events)."""

@@ -3,12 +3,11 @@
 //
 // moe_finalize_unfused needs a [T, H] bf16 workspace between its combine
 // kernel and its shared-add kernel, and expects the caller to provide it.
-// Some callers have no way to do that: code that runs while a CUDA graph is
-// being captured (where cudaMalloc is not allowed), serving engines that
-// plan every device byte before they start and forbid allocation on the
-// request path, and plugins whose host framework owns all device memory and
-// offers them no allocator.  This entry point serves them from a fixed
-// scratch array compiled into the library instead.
+// Some callers have no way to do that: serving engines that plan every
+// device byte before they start and forbid allocation on the request path,
+// and plugins whose host framework owns all device memory and offers them
+// no allocator.  This entry point serves them from a fixed scratch array
+// compiled into the library instead.
 //
 // The array is a file-scope __device__ variable, so every GPU on which the
 // library's device code is loaded holds its kNoallocScratchBytes until the
@@ -31,7 +30,9 @@ constexpr size_t kNoallocScratchBytes = MOEF_NOALLOC_SCRATCH_BYTES;   // 8 MiB
 constexpr int kMaxDevices = 64;
 
 // Device address of g_noalloc_scratch on the current device (looked up once
-// per device; the lookup allocates nothing).
+// per device; the lookup allocates nothing).  The cached address belongs to
+// the device's primary context at the time of the lookup; a context that is
+// destroyed and recreated (cudaDeviceReset) leaves it stale.
 cudaError_t scratch_address(void **out) {
     static std::atomic<void *> cached[kMaxDevices];
     int dev = 0;

@@ -1,6 +1,6 @@
 """moe_finalize_unfused_noalloc, the entry point for callers that cannot
-allocate device memory (inside CUDA-graph capture, engines with a fixed
-memory plan, plugins without an allocator): it must give the same result as
+allocate device memory (engines with a fixed memory plan, plugins without an
+allocator): it must give the same result as
 moe_finalize_unfused with a caller-owned workspace, call after call, even
 though every call reuses one fixed scratch array inside the library.
 
@@ -80,3 +80,24 @@ def test_noalloc_rejects_requests_beyond_its_scratch(cuda_lib):
     with pytest.raises(ValueError):
         cuda_lib.moe_finalize_unfused_noalloc(big["x"], big["idx"], big["w"], "fp32",
                                               big["shared"], out=out)
+
+
+def test_noalloc_at_the_largest_accepted_size(cuda_lib, orc):
+    """T * H * 2 equal to the scratch size exactly (T = 4096 at H = 1024) is
+    accepted and matches both the workspace path, bit for bit, and the
+    oracle within the unfused path's derived tolerance (its intermediate is
+    rounded to bf16)."""
+    from gpu_util import run_oracle
+    from test_unfused import _check
+    H = 1024
+    T = (8 << 20) // (2 * H)
+    wl = W.synth("noalloc_max", T=T, K=4, H=H, E=2048, tile=32, P=32 * 2048,
+                 weight_rule="sigmoid", routed_scale=2.5, seed=5, require_all=False)
+    assert T * H * 2 == 8 << 20
+    dev = to_device(wl)
+    ref = _with_workspace(cuda_lib, wl, dev)
+    out = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert _raw_noalloc(cuda_lib, wl, dev, {"out": out}) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(out), bits_of(ref["out"]))
+    _check({"out": out}, run_oracle(orc, wl), wl, "noalloc at 8 MiB: ")
