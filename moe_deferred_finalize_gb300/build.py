@@ -42,11 +42,24 @@ def _stale():
 
 
 def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile (if needed) and return the path of libmoe_finalize.so."""
+    """Compile (if needed) and return the path of libmoe_finalize.so.
+    Concurrent builds (several processes finding the library out of date at
+    once) are serialised by a lock file, so none of them reads another's
+    half-written objects."""
     if not force and not _stale():
         build_fastcall()
         return LIB
+    import fcntl
     os.makedirs(OBJ_DIR, exist_ok=True)
+    with open(os.path.join(OBJ_DIR, "build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not _stale():      # another process built it meanwhile
+            build_fastcall()
+            return LIB
+        return _build_locked(verbose, extra_flags)
+
+
+def _build_locked(verbose, extra_flags) -> str:
     nvcc = _nvcc()
 
     def compile_one(src):

@@ -98,8 +98,9 @@ constexpr int kRouteWarps = 4;
 // float gives a larger key, equal floats (-0 and +0 too) equal keys; every
 // key is above 0, which marks "no candidate".
 __device__ __forceinline__ uint32_t order_key(float v) {
-    const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t u = __float_as_uint(v + 0.f);   // -0 + 0 = +0 (round to nearest)
+    // sign set: all bits flipped; sign clear: the sign bit set
+    return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
 __device__ __forceinline__ float key_value(uint32_t k) {
@@ -127,22 +128,50 @@ __device__ __forceinline__ void lane_best2(const uint32_t (&key)[EPL], uint32_t 
     }
 }
 
-template <int EPL>
+// Slot j of lane l holds expert id(l, j): with CONTIG (E = 32 * EPL, every
+// lane full) the lane's block l * EPL + j, read with 16-byte loads when VEC4;
+// otherwise the strided l + 32 * j, so that E >= K logits always sit on at
+// least K lanes (the threshold below relies on it).
+template <int EPL, bool CONTIG>
+__device__ __forceinline__ int slot_id(int lane, int j) {
+    return CONTIG ? lane * EPL + j : lane + 32 * j;
+}
+
+template <int EPL, bool CONTIG>
+__device__ __forceinline__ int slot_lane(uint32_t id) {
+    return CONTIG ? static_cast<int>(id / EPL) : static_cast<int>(id & 31u);
+}
+
+// KT: K when fixed at compile time (the common top-8), else 0 (K from Kp).
+template <int EPL, bool CONTIG, bool VEC4, int KT>
 __global__ void __launch_bounds__(kRouteWarps * 32)
-topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kind,
+topk_route_kernel(const float *__restrict__ logits, int T, int E, int Kp, int kind,
                   int32_t *__restrict__ expert_ids, float *__restrict__ weights,
                   int32_t *__restrict__ packed) {
     __shared__ uint64_t s_cand[kRouteWarps][32];   // candidates, then the kept ones by rank
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int K = KT ? KT : Kp;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
     if (t >= T) return;                 // whole warps leave together
     const float *z = logits + static_cast<int64_t>(t) * E;
     uint32_t key[EPL];
+    if constexpr (VEC4) {
+        const float4 *z4 = reinterpret_cast<const float4 *>(z + lane * EPL);
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-        const int e = lane + 32 * j;
-        key[j] = e < E ? order_key(__ldg(z + e)) : 0u;
+        for (int q = 0; q < EPL / 4; ++q) {
+            const float4 f = __ldg(z4 + q);
+            key[4 * q + 0] = order_key(f.x);
+            key[4 * q + 1] = order_key(f.y);
+            key[4 * q + 2] = order_key(f.z);
+            key[4 * q + 3] = order_key(f.w);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int e = slot_id<EPL, CONTIG>(lane, j);
+            key[j] = e < E ? order_key(__ldg(z + e)) : 0u;
+        }
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     uint32_t kept_key = 0u, top_key = 0u;
@@ -187,7 +216,7 @@ topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kin
         for (int j = 0; j < EPL; ++j) {
             if ((cmask >> j) & 1u) {
                 s_cand[w][pos] = (static_cast<uint64_t>(key[j]) << 32) |
-                                 (0xFFFFFFFFu - static_cast<uint32_t>(lane + 32 * j));
+                                 (0xFFFFFFFFu - static_cast<uint32_t>(slot_id<EPL, CONTIG>(lane, j)));
                 ++pos;
             }
         }
@@ -219,10 +248,11 @@ topk_route_kernel(const float *__restrict__ logits, int T, int E, int K, int kin
         for (int k = 0; k < K; ++k) {
             const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, b1);
             const uint32_t wi = __reduce_min_sync(
-                0xFFFFFFFFu, b1 == wk ? static_cast<uint32_t>(lane + 32 * j1) : 0xFFFFFFFFu);
+                0xFFFFFFFFu,
+                b1 == wk ? static_cast<uint32_t>(slot_id<EPL, CONTIG>(lane, j1)) : 0xFFFFFFFFu);
             if (lane == k) { kept_key = wk; kept_id = static_cast<int>(wi); }
             if (k == 0) top_key = wk;
-            if (static_cast<int>(wi & 31u) == lane) {   // this lane's best was taken
+            if (slot_lane<EPL, CONTIG>(wi) == lane) {   // this lane's best was taken
                 taken |= 1u << j1;
                 if (second_known) {
                     b1 = b2;
@@ -262,8 +292,8 @@ unsigned grid_for(int64_t n, int num_sms) {
     return static_cast<unsigned>(blocks);
 }
 
-template <int EPL>
-cudaError_t launch_route_t(const float *logits, int T, int E, int K, int kind, int32_t *ids,
+template <int EPL, bool CONTIG, bool VEC4, int KT>
+cudaError_t launch_route_k(const float *logits, int T, int E, int K, int kind, int32_t *ids,
                            float *w, int32_t *packed, cudaStream_t stream) {
     void *args[] = {&logits, &T, &E, &K, &kind, &ids, &w, &packed};
     cudaLaunchAttribute attr[1];
@@ -275,8 +305,26 @@ cudaError_t launch_route_t(const float *logits, int T, int E, int K, int kind, i
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&topk_route_kernel<EPL>),
-                               args);
+    return cudaLaunchKernelExC(
+        &cfg, reinterpret_cast<const void *>(&topk_route_kernel<EPL, CONTIG, VEC4, KT>), args);
+}
+
+// Full rows (E = 32 * EPL) take the contiguous layout, with 16-byte loads
+// when every row starts 16-byte aligned; top-8 routing takes the build with
+// K fixed.
+template <int EPL>
+cudaError_t launch_route_t(const float *logits, int T, int E, int K, int kind, int32_t *ids,
+                           float *w, int32_t *packed, cudaStream_t stream) {
+    const bool full = E == 32 * EPL;
+    const bool vec4 = full && EPL % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) % 16) == 0;
+    if (vec4 && K == 8)
+        return launch_route_k<EPL, true, (EPL % 4 == 0), 8>(logits, T, E, K, kind, ids, w,
+                                                            packed, stream);
+    if (vec4) return launch_route_k<EPL, true, (EPL % 4 == 0), 0>(logits, T, E, K, kind, ids, w,
+                                                                  packed, stream);
+    if (full) return launch_route_k<EPL, true, false, 0>(logits, T, E, K, kind, ids, w, packed,
+                                                        stream);
+    return launch_route_k<EPL, false, false, 0>(logits, T, E, K, kind, ids, w, packed, stream);
 }
 
 }  // namespace
