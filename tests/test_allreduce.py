@@ -329,3 +329,80 @@ def test_tp_orchestration_one_rank(cuda_lib, orc):
         group.close()
     finally:
         dist.destroy_process_group()
+
+
+def _tp_worker(rank, port, steps, q):
+    """One rank of a two-process group on GPU 0: real CUDA IPC buffers and
+    interprocess events, gloo for set-up and the per-step host barrier."""
+    import os
+    import sys
+    import traceback
+    try:
+        root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+        sys.path.insert(0, root)
+        sys.path.insert(0, os.path.join(root, "tests"))
+        import torch
+        import torch.distributed as dist
+        from moe_deferred_finalize_gb300 import tp
+        from moe_deferred_finalize_gb300 import workloads as W2
+        from gpu_util import bf16_dev, bits_of, weights_dev
+        torch.cuda.set_device(0)
+        dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                                world_size=2)
+        try:
+            group = tp.TPFinalize(dist.group.WORLD, 16, 7168)
+            got = []
+            for T, seed in steps:
+                g = W2.tp_decode(2, T, seed=seed)
+                wl = g.ranks[rank]
+                x = {"permuted_out": bf16_dev(wl.permuted_out),
+                     "idx_map": torch.from_numpy(wl.idx).cuda(), "weights": weights_dev(wl),
+                     "shared_out": bf16_dev(wl.shared)}
+                outs = {k: torch.empty((T, 7168), dtype=torch.bfloat16, device="cuda")
+                        for k in ("out", "residual_out", "norm_out")}
+                group.step(x, g.wkind, g.routed_scale, T, residual=bf16_dev(g.residual),
+                           gamma=bf16_dev(g.gamma), eps=g.eps, outs=outs)
+                torch.cuda.synchronize()
+                got.append({k: bits_of(v) for k, v in outs.items()})
+            group.close()
+            q.put((rank, "ok", got))
+        finally:
+            dist.destroy_process_group()
+    except Exception:
+        q.put((rank, "error", traceback.format_exc()))
+
+
+def test_tp_orchestration_two_processes_one_gpu(cuda_lib, orc):
+    """The two-phase orchestration with two processes sharing one GPU: each
+    opens the other's partial buffers and events through CUDA IPC, and its
+    stream waits on the other's events (no kernel waits on another).  Three
+    steps of different token counts; both ranks' outputs equal bit for bit
+    and match the oracle of the whole group."""
+    import socket
+    import torch.multiprocessing as tmp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    steps = [(16, 41), (1, 42), (16, 43)]
+    ctx = tmp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_tp_worker, args=(r, port, steps, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(2):
+        rank, status, payload = q.get(timeout=300)
+        got[rank] = (status, payload)
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    for rank in (0, 1):
+        assert got[rank][0] == "ok", got[rank][1]
+    for i, (T, seed) in enumerate(steps):
+        a, b = got[0][1][i], got[1][1][i]
+        for key in a:
+            assert np.array_equal(a[key], b[key]), (T, key)
+        ref = oracle_ar(orc, W.tp_decode(2, T, seed=seed))
+        for key in ref:
+            f = (a[key].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            assert_close(f, ref[key], f"two processes, step {i} (T={T}) {key}")
