@@ -440,6 +440,11 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
         if (nvc > 32) nvc = round_up(nvc, 32);
         if (nvc > nvc_max) nvc = nvc_max;
     }
+    // whole warps (the RMSNorm epilogue reduces with full-warp shuffles):
+    // R * nvc a multiple of 32
+    int unit = 32;
+    while (unit > 1 && R % 2 == 0 && (unit / 2) * R % 32 == 0) unit /= 2;
+    nvc = round_up(nvc, unit);
     splits = ceil_div(nvec, slice);   // no empty CTAs
     const int64_t grid = static_cast<int64_t>(T) * splits;
     if (grid > 0x7FFFFFFFLL) return MOEF_ERR_SHAPE;

@@ -290,6 +290,7 @@ def test_allreduce_plans(mf):
                             continue
                         nvec = H // p["vec"]
                         assert p["lanes"] == R and p["threads"] == R * p["nvc"] <= 512
+                        assert p["threads"] % 32 == 0          # whole warps: full-mask shuffles
                         assert p["splits"] * p["slice"] >= nvec > (p["splits"] - 1) * p["slice"]
                         assert p["passes"] * p["nvc"] >= p["slice"]
                         assert p["grid"] == T * p["splits"]

@@ -98,6 +98,8 @@ CASES = [
     (4, 400, 8, 7168, "fp32", True),     # large T: split halved, several passes
     (8, 300, 8, 2048, "packed", True),
     (7, 33, 5, 5120, "fp32", False),
+    (3, 5, 2, 64, "fp32", True),         # a row shorter than a warp per rank: padded to whole warps
+    (5, 2, 3, 40, "bf16", True),         # scalar path, 5 ranks, 40 values a row
 ]
 
 

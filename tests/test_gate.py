@@ -23,6 +23,7 @@ def _logits(T, E, seed, ties=False):
 
 
 @pytest.mark.parametrize("T,E,K", [(1, 256, 8), (3, 8, 8), (256, 256, 8), (4100, 384, 8),
+                                   (5, 256, 8), (1023, 256, 8), (17, 256, 7), (9, 256, 16),
                                    (5, 1000, 32), (7, 33, 1), (64, 64, 6), (2, 1024, 16)])
 @pytest.mark.parametrize("kind", ["softmax", "sigmoid"])
 def test_gate_matches_oracle(cuda_lib, orc, T, E, K, kind):
@@ -134,3 +135,27 @@ def test_gate_candidate_count_boundary(cuda_lib, orc, n_top):
         assert np.array_equal(ids, rid), (n_top, kind)
         assert np.allclose(res["weights"].cpu().numpy(), rw, rtol=2e-6, atol=1e-9)
         assert np.array_equal(ids[0], np.arange(8))
+
+
+def test_gate_warp_with_mixed_tokens(cuda_lib, orc):
+    """Top-8 of 256 takes four tokens per warp; tokens with many equal
+    largest logits (more candidates than one segment can rank) sit in the
+    same warps as ordinary ones, and the last warp holds fewer than four
+    tokens.  Every token must still match the oracle."""
+    rng = np.random.default_rng(77)
+    T = 13
+    z = rng.standard_normal((T, 256)).astype(np.float32)
+    for t in range(T):
+        if t % 5 == 2:
+            z[t, rng.choice(256, 40, replace=False)] = 4.0    # 40 equal maxima
+    z[7, :] = 1.5                                             # every logit equal
+    for kind in ("softmax", "sigmoid"):
+        res = cuda_lib.topk_route(torch.from_numpy(z).cuda(), 8, kind, want_packed=True)
+        torch.cuda.synchronize()
+        rid, rw = orc.topk_route(z, 8, kind)
+        ids = res["expert_ids"].cpu().numpy()
+        assert np.array_equal(ids, rid), kind
+        assert np.array_equal(ids[7], np.arange(8))
+        assert np.allclose(res["weights"].cpu().numpy(), rw, rtol=2e-6, atol=1e-9)
+        assert np.array_equal(res["packed"].cpu().numpy(),
+                              orc.pack_topk_ids(ids, res["weights"].cpu().numpy()))
