@@ -367,7 +367,25 @@ def _tp_worker(rank, port, steps, q):
                 torch.cuda.synchronize()
                 got.append({k: bits_of(v) for k, v in outs.items()})
             group.close()
-            q.put((rank, "ok", got))
+            # the one-shot form over shared input sets (room for the largest buffer)
+            one = tp.TPFinalize(dist.group.WORLD, 16, 7168, one_shot=(2048, 8, "fp32"))
+            shots = []
+            for T, seed in steps:
+                g = W2.tp_decode(2, T, seed=seed)
+                wl = g.ranks[rank]
+                x = one.inputs()
+                x["permuted_out"][:wl.P].copy_(bf16_dev(wl.permuted_out))
+                x["idx_map"][:T].copy_(torch.from_numpy(wl.idx))
+                x["weights"][:T].copy_(weights_dev(wl))
+                x["shared_out"][:T].copy_(bf16_dev(wl.shared))
+                outs = {k: torch.empty((T, 7168), dtype=torch.bfloat16, device="cuda")
+                        for k in ("out", "residual_out", "norm_out")}
+                one.step_one_shot(T, routed_scale=g.routed_scale, residual=bf16_dev(g.residual),
+                                  gamma=bf16_dev(g.gamma), eps=g.eps, outs=outs)
+                torch.cuda.synchronize()
+                shots.append({k: bits_of(v) for k, v in outs.items()})
+            one.close()
+            q.put((rank, "ok", (got, shots)))
         finally:
             dist.destroy_process_group()
     except Exception:
@@ -375,11 +393,12 @@ def _tp_worker(rank, port, steps, q):
 
 
 def test_tp_orchestration_two_processes_one_gpu(cuda_lib, orc):
-    """The two-phase orchestration with two processes sharing one GPU: each
-    opens the other's partial buffers and events through CUDA IPC, and its
-    stream waits on the other's events (no kernel waits on another).  Three
-    steps of different token counts; both ranks' outputs equal bit for bit
-    and match the oracle of the whole group."""
+    """The orchestration with two processes sharing one GPU: each opens the
+    other's buffers and events through CUDA IPC, and its stream waits on the
+    other's events (no kernel waits on another).  Three two-phase steps of
+    different token counts, then the same three as one-shot steps over the
+    shared input sets: every output of both ranks in both forms equal bit for
+    bit, and matching the oracle of the whole group."""
     import socket
     import torch.multiprocessing as tmp
     with socket.socket() as s:
@@ -401,9 +420,12 @@ def test_tp_orchestration_two_processes_one_gpu(cuda_lib, orc):
     for rank in (0, 1):
         assert got[rank][0] == "ok", got[rank][1]
     for i, (T, seed) in enumerate(steps):
-        a, b = got[0][1][i], got[1][1][i]
+        a, b = got[0][1][0][i], got[1][1][0][i]
         for key in a:
             assert np.array_equal(a[key], b[key]), (T, key)
+            # the one-shot form on both ranks: bit-identical to the two-phase
+            for rank in (0, 1):
+                assert np.array_equal(got[rank][1][1][i][key], a[key]), (T, key, rank)
         ref = oracle_ar(orc, W.tp_decode(2, T, seed=seed))
         for key in ref:
             f = (a[key].astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -63,3 +63,58 @@ def test_fuzz_case(cuda_lib, orc, i):
                                 threads=c["threads"], **kw)
     torch.cuda.synchronize()
     compare(res, run_oracle(orc, wl), f"case {i} {c}: ")
+
+
+N_AR_CASES = 40
+
+
+def _ar_case(i):
+    rng = np.random.default_rng(5000 + i)
+    R = int(rng.integers(1, 9))
+    K = int(rng.choice([1, 2, 3, 4, 8, 9, 16, 32]))
+    T = int(rng.integers(1, max(2, 600 // (R * K) + 2)))
+    H = int(rng.choice([8, 64, 136, 1024, 7168, int(rng.integers(1, 2049))]))
+    return dict(R=R, T=T, K=K, H=H, wkind=str(rng.choice(["fp32", "bf16", "packed"])),
+                norm=bool(rng.integers(2)), unaligned=bool(rng.random() < 0.25),
+                in_place=bool(rng.random() < 0.25), scale=float(rng.choice([1.0, 2.5, 0.5])),
+                seed=i)
+
+
+@pytest.mark.parametrize("i", range(N_AR_CASES))
+def test_fuzz_allreduce_case(cuda_lib, orc, i):
+    """The all-reduce-fused finalize over random rank counts, sizes,
+    encodings, epilogues, unaligned operands and in-place residuals: the
+    one-shot against the oracle, the two-phase form bit-identical to it."""
+    from test_allreduce import oracle_ar
+    c = _ar_case(i)
+    R, T, K, H = c["R"], c["T"], c["K"], c["H"]
+    nb = max(K + 1, (T * K + 7) // 8)
+    g = W.tp_group("fuzz_ar", R, T=T, K=K, H=H, E=2 * nb + 64, tile=32, P=nb * 32,
+                   wkind=c["wkind"], routed_scale=c["scale"], with_norm=c["norm"],
+                   seed=c["seed"])
+    move = _unaligned if c["unaligned"] else (lambda t: t)
+    ranks = []
+    for wl in g.ranks:
+        d = to_device(wl)
+        ranks.append({"permuted_out": move(d["x"]), "idx_map": d["idx"], "weights": d["w"],
+                      "shared_out": move(d["shared"])})
+    ep = {}
+    if g.with_norm:
+        ep = {"residual": move(bf16_dev(g.residual)), "gamma": move(bf16_dev(g.gamma)),
+              "eps": g.eps}
+        if c["in_place"]:
+            ep["residual_out"] = ep["residual"]
+    ref = oracle_ar(orc, g)
+    a = cuda_lib.moe_finalize_allreduce(ranks, g.wkind, routed_scale=g.routed_scale, **ep)
+    torch.cuda.synchronize()
+    compare(a, ref, f"case {i} {c}: ")
+    if c["in_place"] and g.with_norm:
+        return                      # the residual has been overwritten
+    parts = [cuda_lib.moe_finalize_partial(r["permuted_out"], r["idx_map"], r["weights"],
+                                           g.wkind, r["shared_out"], routed_scale=g.routed_scale)
+             for r in ranks]
+    b = cuda_lib.moe_finalize_allreduce_reduce(parts, **ep)
+    torch.cuda.synchronize()
+    for key in a:
+        if a[key] is not None:
+            assert torch.equal(a[key].view(torch.int16), b[key].view(torch.int16)), (i, key)

@@ -37,28 +37,33 @@ class ShmTransport:
     events are log entries, since the stand-in kernels run synchronously."""
 
     def __init__(self, rank, log):
-        self.rank, self.log, self.segments, self.n = rank, log, [], 0
+        self.rank, self.log, self.segments, self.created, self.n = rank, log, [], [], 0
+
+    # bf16 buffers hold raw bit patterns here
+    NP = {torch.float32: np.float32, torch.int32: np.int32, torch.bfloat16: np.uint16}
 
     def alloc(self, shape, dtype):
         from multiprocessing import shared_memory
-        assert dtype == torch.float32
-        seg = shared_memory.SharedMemory(create=True, size=int(np.prod(shape)) * 4)
+        nd = np.dtype(self.NP[dtype])
+        seg = shared_memory.SharedMemory(create=True, size=int(np.prod(shape)) * nd.itemsize)
         self.segments.append(seg)
-        arr = np.ndarray(shape, np.float32, buffer=seg.buf)
-        arr[:] = np.nan
+        self.created.append(seg)
+        arr = np.ndarray(shape, nd, buffer=seg.buf)
+        arr[:] = 0
         return torch.from_numpy(arr)
 
     def export(self, t):
+        a = t.numpy()
         seg = next(s for s in self.segments
-                   if np.shares_memory(np.ndarray(t.shape, np.float32, buffer=s.buf), t.numpy()))
-        return (seg.name, tuple(t.shape))
+                   if np.shares_memory(np.ndarray(s.size, np.uint8, buffer=s.buf), a))
+        return (seg.name, tuple(t.shape), a.dtype.str)
 
     def open(self, handle):
         from multiprocessing import shared_memory
-        name, shape = handle
+        name, shape, dt = handle
         seg = shared_memory.SharedMemory(name=name)
         self.segments.append(seg)
-        return torch.from_numpy(np.ndarray(shape, np.float32, buffer=seg.buf))
+        return torch.from_numpy(np.ndarray(shape, np.dtype(dt), buffer=seg.buf))
 
     def new_event(self):
         self.n += 1
@@ -83,8 +88,12 @@ class ShmTransport:
         self.log.append(("synchronize",))
 
     def close(self):
+        """Called after the group's closing barrier: no peer maps a segment
+        any more, so the creator may remove it."""
         for s in self.segments:
             s.close()
+        for s in self.created:
+            s.unlink()
 
 
 class OracleBackend:
@@ -106,6 +115,13 @@ class OracleBackend:
         outs["norm_out"] = torch.nn.functional.rms_norm(torch.from_numpy(s), (s.shape[1],),
                                                         weight=g, eps=eps).numpy()
         self.log.append(("reduce", len(partials)))
+
+    def one_shot(self, ranks, wkind, scale, residual, gamma, eps, outs, stream):
+        rk = [{"permuted_out": r["permuted_out"].numpy(), "idx": r["idx_map"].numpy(),
+               "weights": r["weights"].numpy(), "shared": r["shared_out"].numpy()}
+              for r in ranks]
+        outs.update(self.orc.moe_finalize_ar(rk, wkind, scale, residual, gamma, eps))
+        self.log.append(("one_shot", len(ranks)))
 
 
 def _group():
@@ -146,7 +162,26 @@ def _worker(rank, port, q, bad_h):
                 results.append({k: np.asarray(v) for k, v in outs.items()})
             group.close()
             assert log[-1] == ("synchronize",) and group.buffers is None
-            q.put((rank, "ok", (results, log)))
+            log_two_phase = list(log)
+            # the one-shot form: every rank fills its shared input set, then one
+            # launch per rank reads all of them
+            del log[:]
+            g0 = _group()[0]
+            one = tp.TPFinalize(dist.group.WORLD, MAX_T, H, transport=transport,
+                                backend=OracleBackend(oracle.default(), log),
+                                one_shot=(g0.ranks[0].P, K, "fp32"))
+            shots = []
+            for g in _group():
+                wl = g.ranks[rank]
+                x = one.inputs()
+                x["permuted_out"].numpy()[:] = wl.permuted_out
+                x["idx_map"].numpy()[:g.T] = wl.idx
+                x["weights"].numpy()[:g.T] = wl.weights
+                x["shared_out"].numpy()[:g.T] = wl.shared
+                shots.append(one.step_one_shot(g.T, routed_scale=g.routed_scale,
+                                               residual=g.residual, gamma=g.gamma, eps=g.eps))
+            one.close()
+            q.put((rank, "ok", (results, log_two_phase, shots, list(log))))
         finally:
             transport.close()
             dist.destroy_process_group()
@@ -177,7 +212,21 @@ def test_two_phase_protocol_and_results_gloo(orc):
         assert got[rank][0] == "ok", got[rank][1]
     groups = _group()
     for rank in (0, 1):
-        results, log = got[rank][1]
+        results, log, shots, log_one = got[rank][1]
+        # one-shot steps: record this step's event, wait on the peer's, one launch
+        # (the one-shot group's events are the transport's third and fourth)
+        for s, T in enumerate(STEPS):
+            b = 2 + s % 2
+            assert log_one[3 * s:3 * s + 3] == [("record", rank, b), ("wait", 1 - rank, b),
+                                                ("one_shot", 2)], log_one
+        for g, res in zip(_group(), shots):
+            ranks = [{"permuted_out": wl.permuted_out, "idx": wl.idx, "weights": wl.weights,
+                      "shared": wl.shared} for wl in g.ranks]
+            ref = orc.moe_finalize_ar(ranks, g.wkind, g.routed_scale, g.residual, g.gamma,
+                                      g.eps)
+            for key in ref:
+                # the stand-in launch is the oracle over the shared input sets
+                assert np.array_equal(res[key], ref[key]), (g.name, key)
         # per step: phase 1 into buffer (step % 2), record that buffer's event,
         # wait on the peer's event of the same buffer, reduce over both ranks
         peer = 1 - rank
