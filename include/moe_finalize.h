@@ -396,13 +396,16 @@ moef_status moe_finalize_allreduce_reduce(const float *const *partials, int R,
                                           int T, int H, cudaStream_t stream);
 
 /*
- * Launch plan of the all-reduce-fused kernels.  A CTA holds `lanes` groups
- * of `nvc` threads (threads = lanes * nvc); in one pass thread j of group r
- * obtains rank r's partial of vector j of the CTA's slice, and group 0 sums
- * the ranks and finishes the vector.  Each token row is cut into `splits`
- * slices of `slice` vectors of `vec` values, taken in `passes` passes; with
- * a residual and splits > 1 the CTAs of a token form a cluster of `cluster`
- * CTAs.  smem_bytes: dynamic shared memory per CTA.
+ * Launch plan of the all-reduce-fused kernels.  A one-shot CTA holds `lanes`
+ * groups of `nvc` threads (threads = lanes * nvc; lanes divides R); in one
+ * pass thread j of group g obtains the partials of vector j of the CTA's
+ * slice for the R / lanes consecutive ranks from g * R / lanes on, and
+ * thread j of group 0 sums all ranks in rank order and finishes the vector.
+ * Each token row is cut into `splits` slices of `slice` vectors of `vec`
+ * values, taken in `passes` passes; with a residual and splits > 1 the CTAs
+ * of a token form a cluster of `cluster` CTAs.  Phase 2 runs the nvc
+ * finishing threads alone (rounded up to whole warps), over the same
+ * vectors.  smem_bytes: dynamic shared memory per one-shot CTA.
  */
 typedef struct {
     int vec;
@@ -419,8 +422,9 @@ typedef struct {
 
 /*
  * moe_finalize_allreduce_plan -- the plan of the one-shot and phase-2 calls
- * (lanes = R; the two share it, which keeps their results bit-identical),
- * or of phase 1 with R = 1 and with_norm = 0.  Pure host computation.
+ * (the two share it, which keeps their results bit-identical: lanes = R at
+ * decode sizes, R / 2 from 5 tokens on when R > 4, 1 from 64 tokens on), or
+ * of phase 1 with R = 1 and with_norm = 0.  Pure host computation.
  * Returns MOEF_ERR_SHAPE when an RMSNorm row is too long for one cluster
  * (more than 16 CTAs x 8 passes), else as moe_finalize_plan.
  */

@@ -378,6 +378,27 @@ namespace {
 constexpr int kArMaxThreads = 512;    // the all-reduce kernels' launch bounds
 constexpr int kArMaxPasses = 8;
 
+// Tokens from which the ranks of a vector are summed in sequence by one
+// thread (lanes = 1), and the vectors of such a plan's slice.
+#ifndef MOEF_AR_SEQ_MIN_TOKENS
+#define MOEF_AR_SEQ_MIN_TOKENS 64
+#endif
+#ifndef MOEF_AR_SEQ_SLICE
+#define MOEF_AR_SEQ_SLICE 128
+#endif
+// Largest rank group count from 5 tokens on (R > this: groups of 2 ranks).
+#ifndef MOEF_AR_MID_LANES
+#define MOEF_AR_MID_LANES 4
+#endif
+constexpr int kArSeqMinTokens = MOEF_AR_SEQ_MIN_TOKENS;
+constexpr int kArSeqSlice = MOEF_AR_SEQ_SLICE;
+// Largest CTA of a sequential-ranks plan with RMSNorm.
+#ifndef MOEF_AR_SEQ_MAX_THREADS
+#define MOEF_AR_SEQ_MAX_THREADS 256
+#endif
+constexpr int kArMidLanes = MOEF_AR_MID_LANES;
+constexpr int kArSeqMaxThreads = MOEF_AR_SEQ_MAX_THREADS;
+
 int pow2_bucket(int need) {
     int b = 1;
     while (b < need) b *= 2;
@@ -386,21 +407,33 @@ int pow2_bucket(int need) {
 
 }  // namespace
 
-// Plan of the all-reduce-fused kernels.  A CTA holds R groups of threads,
-// one per rank, each thread obtaining one rank's partial of one vector per
-// pass, so that decode-size calls keep every rank's row loads in flight at
-// once:
-//  * without RMSNorm, 128 threads per CTA (R groups of 128 / R, at least 16
-//    threads), one vector per thread: slices of 128 / R vectors;
+// Plan of the all-reduce-fused kernels.  At decode sizes a CTA holds R
+// groups of threads, one per rank, each thread obtaining one rank's partial
+// of one vector per pass, so that every rank's row loads are in flight at
+// once (lanes = R); from 5 tokens on, with more than kArMidLanes ranks and
+// 16-byte vectors, R / 2 groups of two ranks each:
+//  * without RMSNorm, 128 threads per CTA (`lanes` groups of 128 / lanes, at
+//    least 16 threads), one vector per thread: slices of 128 / lanes vectors;
 //  * with RMSNorm, one CTA or one cluster of up to 16 CTAs finishes a row.
 //    Each extra pass over a slice costs a full chain of loads, barrier and
 //    epilogue (about 2.8 us at R = 8, T = 1), so a few tokens take CTAs of
-//    up to 512 threads (R groups of 512 / R, at most 256), enough for one
+//    up to 512 threads (`lanes` groups of 512 / lanes, at most 256), enough for one
 //    pass: with R = 8 at H = 7168, 14 CTAs of 8 x 64 threads.  From T = 5 on
 //    CTAs of 256 threads win even with a second pass (R = 4, T = 16: 14 x
 //    256 threads 5.6 us vs 7 x 512 threads 9.3 us; R = 8: 16 x 224 threads
 //    9.2 us vs 14 x 512 threads 11.9 us).  The split is halved while the grid
 //    exceeds 4 CTAs per SM, each thread then taking up to 8 passes.
+// With many tokens (R > 1, T >= kArSeqMinTokens, 16-byte vectors) the
+// tokens alone fill the GPU, and each thread sums the ranks of its vector in
+// sequence (lanes = 1).  Slices start at kArSeqSlice vectors, one pass each;
+// with RMSNorm a row is one cluster of up to 16 CTAs of up to 256 threads,
+// the split halved while the grid exceeds 4 CTAs per SM (fewer, larger
+// clusters: R = 8, T = 256: 2 CTAs x 2 passes of 224 threads per row, 46.3
+// us against 47.9 us for 7 CTAs of 128 threads), up to 8 passes.  Measured
+// on GB300 at H = 7168 (one-shot / two-phase per rank, us): R = 8, T = 16:
+// rank pairs 8.9 / 6.5, one rank per group 9.2 / 8.5; T = 32: rank pairs
+// 11.1 / 7.7, one rank per group 15.3 / 8.8, sequential 17.2 / 8.0; T = 64:
+// sequential 18.9 / 9.2, one rank per group 19.1 / 12.8.
 moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int vec_ok,
                                         int num_sms, moef_ar_plan *plan) {
     if (!plan) return MOEF_ERR_NULL;
@@ -409,52 +442,88 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
     const int vec = (vec_ok && H % 8 == 0) ? 8 : 1;
     const int nvec = H / vec;
     const int64_t rows = T > 0 ? T : 1;
-    int nvc, splits, slice, passes;
-    if (!with_norm) {
-        nvc = 128 / R / 16 * 16;
-        if (nvc < 16) nvc = 16;
-        if (nvc > nvec) nvc = nvec;
-        slice = nvc;
-        splits = ceil_div(nvec, slice);
-        if (rows * splits > 0x7FFFFFFFLL) {
-            splits = static_cast<int>(0x7FFFFFFFLL / rows);
-            if (splits < 1) splits = 1;
+    int lanes = R, nvc = 0, splits = 0, slice = 0, passes = 0;
+    if (R > 1 && vec == 8 && T >= kArSeqMinTokens) {
+        lanes = 1;
+        if (!with_norm) {
+            nvc = kArSeqSlice < nvec ? kArSeqSlice : nvec;
+            slice = nvc;
+            splits = ceil_div(nvec, slice);
+            if (rows * splits > 0x7FFFFFFFLL) {
+                splits = static_cast<int>(0x7FFFFFFFLL / rows);
+                if (splits < 1) splits = 1;
+                slice = ceil_div(nvec, splits);
+            }
+            passes = ceil_div(slice, nvc);
+        } else {
+            splits = ceil_div(nvec, kArSeqSlice);
+            if (splits > kMaxCluster) splits = kMaxCluster;
+            while (splits > 1 && rows * splits > 4 * static_cast<int64_t>(num_sms)) {
+                const int half = ceil_div(splits, 2);
+                if (ceil_div(ceil_div(nvec, half), kArSeqMaxThreads) > kArMaxPasses) break;
+                splits = half;
+            }
             slice = ceil_div(nvec, splits);
+            passes = pow2_bucket(ceil_div(slice, kArSeqMaxThreads));
+            if (passes > kArMaxPasses) {
+                lanes = R;                   // too long a row: the rank-group plan decides
+            } else {
+                nvc = round_up(ceil_div(slice, passes), 32);
+                if (nvc > kArSeqMaxThreads) nvc = kArSeqMaxThreads;
+            }
         }
-        passes = ceil_div(slice, nvc);
-    } else {
-        int nvc_max = (T <= 4 ? kArMaxThreads : kArMaxThreads / 2) / R;
-        if (nvc_max > 256) nvc_max = 256;
-        nvc_max = nvc_max / 32 * 32;
-        splits = ceil_div(nvec, nvc_max);
-        if (splits > kMaxCluster) splits = kMaxCluster;
-        if (ceil_div(ceil_div(nvec, splits), nvc_max) > kArMaxPasses) return MOEF_ERR_SHAPE;
-        while (splits > 1 && rows * splits > 4 * static_cast<int64_t>(num_sms)) {
-            const int half = ceil_div(splits, 2);
-            if (ceil_div(ceil_div(nvec, half), nvc_max) > kArMaxPasses) break;
-            splits = half;
+    }
+    if (lanes > 1 || R == 1) {
+        if (T > 4 && R > kArMidLanes && R % 2 == 0 && vec == 8) lanes = R / 2;
+        if (!with_norm) {
+            nvc = 128 / lanes / 16 * 16;
+            if (nvc < 16) nvc = 16;
+            if (nvc > nvec) nvc = nvec;
+            slice = nvc;
+            splits = ceil_div(nvec, slice);
+            if (rows * splits > 0x7FFFFFFFLL) {
+                splits = static_cast<int>(0x7FFFFFFFLL / rows);
+                if (splits < 1) splits = 1;
+                slice = ceil_div(nvec, splits);
+            }
+            passes = ceil_div(slice, nvc);
+        } else {
+            int nvc_max = (T <= 4 ? kArMaxThreads : kArMaxThreads / 2) / lanes;
+            if (nvc_max > 256) nvc_max = 256;
+            nvc_max = nvc_max / 32 * 32;
+            splits = ceil_div(nvec, nvc_max);
+            if (splits > kMaxCluster) splits = kMaxCluster;
+            if (ceil_div(ceil_div(nvec, splits), nvc_max) > kArMaxPasses) return MOEF_ERR_SHAPE;
+            while (splits > 1 && rows * splits > 4 * static_cast<int64_t>(num_sms)) {
+                const int half = ceil_div(splits, 2);
+                if (ceil_div(ceil_div(nvec, half), nvc_max) > kArMaxPasses) break;
+                splits = half;
+            }
+            slice = ceil_div(nvec, splits);
+            passes = pow2_bucket(ceil_div(slice, nvc_max));
+            nvc = ceil_div(slice, passes);
+            if (nvc > 32) nvc = round_up(nvc, 32);
+            if (nvc > nvc_max) nvc = nvc_max;
         }
-        slice = ceil_div(nvec, splits);
-        passes = pow2_bucket(ceil_div(slice, nvc_max));
-        nvc = ceil_div(slice, passes);
-        if (nvc > 32) nvc = round_up(nvc, 32);
-        if (nvc > nvc_max) nvc = nvc_max;
     }
     // whole warps (the RMSNorm epilogue reduces with full-warp shuffles):
-    // R * nvc a multiple of 32
+    // lanes * nvc a multiple of 32
     int unit = 32;
-    while (unit > 1 && R % 2 == 0 && (unit / 2) * R % 32 == 0) unit /= 2;
+    while (unit > 1 && lanes % 2 == 0 && (unit / 2) * lanes % 32 == 0) unit /= 2;
     nvc = round_up(nvc, unit);
     splits = ceil_div(nvec, slice);   // no empty CTAs
     const int64_t grid = static_cast<int64_t>(T) * splits;
     if (grid > 0x7FFFFFFFLL) return MOEF_ERR_SHAPE;
     const int vbytes = vec == 8 ? 16 : 2;
-    int64_t smem = (R > 1 ? static_cast<int64_t>(sizeof(float)) * vec * R * nvc : 0) +
+    // the exchanged partials of a pass: every group's with one rank per group,
+    // ranks 2 .. R-1 with pairs, none when one thread sums all ranks
+    const int exchanged = lanes == R ? (lanes > 1 ? R : 0) : lanes > 1 ? R - 2 : 0;
+    int64_t smem = static_cast<int64_t>(sizeof(float)) * vec * exchanged * nvc +
                    (with_norm ? static_cast<int64_t>(passes) * nvc * vbytes : 0);
     plan->vec = vec;
-    plan->lanes = R;
+    plan->lanes = lanes;
     plan->nvc = nvc;
-    plan->threads = R * nvc;
+    plan->threads = lanes * nvc;
     plan->splits = splits;
     plan->slice = slice;
     plan->passes = passes;
@@ -524,6 +593,7 @@ moef_status launch_ar(moef::ArParams &p, int R, int T, int H, bool norm, bool ve
     if (st != MOEF_OK) return st;
     p.H = H;
     p.nvec = H / plan.vec;
+    p.ranks = R;
     p.lanes = plan.lanes;
     p.nvc = plan.nvc;
     p.splits = plan.splits;

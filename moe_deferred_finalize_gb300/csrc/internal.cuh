@@ -56,7 +56,8 @@ struct ArParams {
     int wkind;
     int K, H;
     int nvec;                                   // vectors per row
-    int lanes;                                  // thread groups per CTA (ranks summed)
+    int ranks;                                  // R: ranks summed (1 in phase 1)
+    int lanes;                                  // thread groups per CTA: R, or 1
     int nvc;                                    // threads per group = vectors per pass
     int splits;                                 // CTAs per token
     int slice;                                  // vectors per CTA

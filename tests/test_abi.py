@@ -276,8 +276,10 @@ def test_allreduce_argument_errors(mf):
 
 def test_allreduce_plans(mf):
     """Plan invariants over ranks, sizes and both epilogues: R groups of
-    threads per CTA, every vector of a row covered, and with RMSNorm one
-    cluster of at most 16 CTAs and at most 8 passes per thread."""
+    threads per CTA at decode sizes (R / 2 groups of two ranks from 5 tokens
+    on when R > 4; one thread summing all ranks from 64 tokens on), every
+    vector of a row covered, and with RMSNorm one cluster of at most 16 CTAs
+    and at most 8 passes per thread."""
     for R in range(1, 9):
         for H in (8, 64, 100, 1000, 2048, 4104, 7168, 16384, 65536):
             for T in (1, 16, 256, 4096):
@@ -289,7 +291,15 @@ def test_allreduce_plans(mf):
                             assert e.status == 2 and norm
                             continue
                         nvec = H // p["vec"]
-                        assert p["lanes"] == R and p["threads"] == R * p["nvc"] <= 512
+                        # rank groups at decode sizes; each thread summing the
+                        # ranks in sequence once the tokens fill the GPU
+                        seq = R > 1 and p["vec"] == 8 and T >= 64
+                        mid = R // 2 if T > 4 and R > 4 and R % 2 == 0 and p["vec"] == 8 else R
+                        if seq and norm and p["lanes"] == mid:
+                            assert -(-nvec // 16) > 8 * 512      # row too long for one
+                        else:
+                            assert p["lanes"] == (1 if seq else mid)
+                        assert p["threads"] == p["lanes"] * p["nvc"] <= 512
                         assert p["threads"] % 32 == 0          # whole warps: full-mask shuffles
                         assert p["splits"] * p["slice"] >= nvec > (p["splits"] - 1) * p["slice"]
                         assert p["passes"] * p["nvc"] >= p["slice"]
@@ -303,6 +313,11 @@ def test_allreduce_plans(mf):
     # the decode shapes: every rank's loads of a vector in flight in one pass
     p = mf.allreduce_plan(8, 1, 7168, True)
     assert (p["nvc"], p["splits"], p["passes"], p["cluster"]) == (64, 14, 1, 14)
+    # many tokens: one thread per vector summing the 8 ranks, rows in 2
+    # slices of 2 passes over 224 vectors
+    p = mf.allreduce_plan(8, 256, 7168, True)
+    assert (p["lanes"], p["nvc"], p["splits"], p["passes"], p["cluster"], p["grid"]) == \
+        (1, 224, 2, 2, 2, 512)
     with pytest.raises(mf.MoefError):
         mf.allreduce_plan(8, 1, 8 * 8 * 16 * 64 + 8, True)    # longer than 16 CTAs x 8 passes
     with pytest.raises(mf.MoefError):
@@ -326,18 +341,29 @@ def test_allreduce_kernel_indices_stay_in_their_buffers(mf):
                     vec, nvc, lanes, threads = p["vec"], p["nvc"], p["lanes"], p["threads"]
                     nvec = H // vec
                     vbytes = 16 if vec == 8 else 2
-                    sp_bytes = 4 * vec * lanes * nvc if lanes > 1 else 0
+                    c = R // lanes                      # ranks per group
+                    assert c * lanes == R and (c == 1 or vec == 8) and c in (1, 2, R)
+                    # exchanged partials of a pass: every group's (one rank per
+                    # group), ranks 2 .. R-1 (pairs), none (one thread, all ranks)
+                    sp_bytes = 4 * vec * (R if 1 < lanes == R else R - 2 if c == 2 and lanes > 1
+                                          else 0) * nvc
                     keep_bytes = p["passes"] * nvc * vbytes if norm else 0
                     assert sp_bytes + keep_bytes == p["smem_bytes"]
                     assert threads <= 512 and threads // 32 <= 16 and R * 32 <= 256
+                    assert lanes in (1, R, R // 2)
                     for split in range(p["splits"]):
                         v_begin = split * p["slice"]
                         v_end = min(v_begin + p["slice"], nvec)
                         for tid in range(threads):
-                            r, j = divmod(tid, nvc)
-                            assert r < lanes
-                            # partial word (r, j, c) of a pass
-                            assert (r * nvc + j + 1) * vec * 4 <= max(sp_bytes, 4 * vec * nvc)
+                            g, j = divmod(tid, nvc)
+                            assert g < lanes
+                            for rr in range(g * c, g * c + c):
+                                assert rr < R
+                                if lanes == R > 1:    # partial word (rr, j, .) of a pass
+                                    assert (rr * nvc + j + 1) * vec * 4 <= sp_bytes
+                                elif g > 0:           # pairs: word (rr - 2, j, .)
+                                    assert 0 <= (rr - 2) * nvc + j and \
+                                        ((rr - 2) * nvc + j + 1) * vec * 4 <= sp_bytes
                             q = 0
                             for base in range(v_begin, v_end, nvc):
                                 v = base + j
@@ -351,6 +377,24 @@ def test_allreduce_kernel_indices_stay_in_their_buffers(mf):
                                 assert q <= p["passes"]
                     if norm and p["cluster"] > 1:
                         assert p["cluster"] == p["splits"] <= min(16, threads)
+                    # phase 2 (grids above one CTA per SM, or groups of
+                    # several ranks): the nvc finishing threads alone, in whole
+                    # warps, with the kept vectors at the start of shared memory
+                    threads2 = -(-nvc // 32) * 32
+                    assert threads2 <= 512 and (not norm or threads % 32 == 0)
+                    for split in range(p["splits"]):
+                        v_begin = split * p["slice"]
+                        v_end = min(v_begin + p["slice"], nvec)
+                        for j in range(nvc):
+                            q = 0
+                            for base in range(v_begin, v_end, nvc):
+                                if base + j < v_end:
+                                    assert (base + j) * vec + vec <= H
+                                    if norm:
+                                        assert (q * nvc + j + 1) * vbytes <= keep_bytes
+                                q += 1
+                    if norm and p["cluster"] > 1:
+                        assert p["cluster"] <= threads2
 
 
 def test_every_accepted_norm_plan_covers_its_slice_in_one_pass(mf):

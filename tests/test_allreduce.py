@@ -274,26 +274,32 @@ def test_graph_capture_replay(cuda_lib, orc):
 
 
 @pytest.mark.slow
-def test_large_t_sampled_rows(cuda_lib, orc):
-    """T = 1024 with R = 8 at H = 4096 (2-CTA clusters, 8 passes per
-    thread): sampled token rows against the oracle, every row against the
-    two-phase form."""
-    g = W.tp_group("large", 8, T=1024, K=8, H=4096, E=512, tile=64, P=16384,
-                   routed_scale=2.5, seed=9)
-    p = cuda_lib.allreduce_plan(8, 1024, 4096, True)
-    assert (p["splits"], p["passes"]) == (2, 8)
+@pytest.mark.parametrize("R,T,H,E,tile,P,plan", [
+    # each thread sums the 8 ranks in sequence: one CTA per row, 2 passes
+    (8, 1024, 4096, 512, 64, 16384, dict(lanes=1, splits=1, passes=2, cluster=1)),
+    # 4 groups of two ranks, 4 passes per thread, 8-CTA clusters
+    (8, 48, 16384, 64, 32, 1024, dict(lanes=4, splits=8, passes=4, cluster=8)),
+    # one group per rank, 8 passes per thread, 8-CTA clusters
+    (4, 48, 32768, 64, 32, 1024, dict(lanes=4, splits=8, passes=8, cluster=8)),
+])
+def test_large_sampled_rows(cuda_lib, orc, R, T, H, E, tile, P, plan):
+    """Sizes with long rows or many tokens: sampled token rows against the
+    oracle, every row against the two-phase form."""
+    g = W.tp_group("large", R, T=T, K=8, H=H, E=E, tile=tile, P=P, routed_scale=2.5, seed=9)
+    p = cuda_lib.allreduce_plan(R, T, H, True)
+    assert {k: p[k] for k in plan} == plan
     rd = ranks_dev(g)
     a = one_shot(cuda_lib, g, rd)
     b, _ = two_phase(cuda_lib, g, rd)
-    assert_same_bits(a, b, "T=1024 R=8")
-    rows = np.sort(np.random.default_rng(0).choice(g.T, 48, replace=False))
+    assert_same_bits(a, b, f"T={T} H={H} R={R}")
+    rows = np.sort(np.random.default_rng(0).choice(g.T, min(48, g.T), replace=False))
     sub = W.TPGroup("rows", [W.Workload(**{**wl.__dict__, "T": len(rows), "idx": wl.idx[rows],
                                            "weights": wl.weights[rows],
                                            "shared": wl.shared[rows]}) for wl in g.ranks],
                     g.residual[rows], g.gamma, g.eps)
     ref = oracle_ar(orc, sub)
     for key in ref:
-        assert_close(f64_of(a[key])[rows], ref[key], f"T=1024 sampled {key}")
+        assert_close(f64_of(a[key])[rows], ref[key], f"T={T} H={H} sampled {key}")
 
 
 def test_tp_orchestration_one_rank(cuda_lib, orc):
