@@ -10,7 +10,7 @@
 //   out = bf16(m);  residual_out = bf16(m + residual);
 //   norm_out = bf16(residual_out * rsqrt(mean(residual_out^2) + eps) * gamma)
 //
-// One kernel template serves three entry points:
+// Three kernel templates serve three entry points:
 //   * one-shot (moe_finalize_allreduce): every rank's rows are gathered in
 //     one launch, from local or peer-mapped memory;
 //   * phase 1 (moe_finalize_partial): one rank's p_r, stored in fp32;
@@ -19,26 +19,26 @@
 // The one-shot and the two-phase forms run the same arithmetic in the same
 // order under the same launch plan, so their results are bit-identical.
 //
-// Thread layout of the gathering kernel (one-shot, phase 1): a CTA's threads
-// form `lanes` groups of `nvc` threads, and group g works for the R / lanes
-// consecutive ranks from g * R / lanes on.  In one pass thread (g, j)
-// obtains its ranks' partials of vector j of the CTA's slice one after
-// another (per rank K gathered-row loads, 16 bytes each, plus the
+// Thread layout of the gathering kernels (one-shot, phase 1): a CTA's
+// threads form `lanes` groups of `nvc` threads, and group g works for the
+// R / lanes consecutive ranks from g * R / lanes on.  In one pass thread
+// (g, j) obtains its ranks' partials of vector j of the CTA's slice one
+// after another (per rank K gathered-row loads, 16 bytes each, plus the
 // shared-output load), so a pass keeps `lanes` times as many loads in flight
-// as one thread summing all ranks would.  Group 0 sums its own ranks'
-// partials in registers; the other groups' partials meet it in shared
-// memory, where it adds them in rank order and finishes the vector.  Decode
-// sizes use lanes = R (or R / 2 from 5 tokens on when R > 4); with many
-// tokens, enough vectors to fill the GPU, lanes = 1: each thread sums all
-// ranks itself, with no exchange or barrier per pass.  Phase 2 runs a kernel
-// of its own over the same vector-to-thread map: each finishing thread loads
-// the R fp32 partials of its vector at once.  With RMSNorm the bf16
-// residual_out vectors stay in shared memory for the second pass, and a
-// split row combines its partial sums of squares across the CTAs of a
-// thread-block cluster through distributed shared memory, as in the plain
-// finalize.  The finishing threads, their vectors, passes and warps are the
-// same in every form of one plan, and so is the order of the sum of squares:
-// the forms' results are bit-identical.
+// as one thread summing all ranks would.  The partials meet group 0 in
+// shared memory, where it adds them in rank order and finishes the vector.
+// Decode sizes use lanes = R (or R / 2 from 5 tokens on when R > 4); with
+// many tokens, enough vectors to fill the GPU, lanes = 1: each thread sums
+// all ranks itself, with no exchange or barrier per pass.  Phase 2 of a
+// one-rank-per-group plan runs in the same groups over the fp32 partials;
+// phase 2 of the other plans runs a kernel of its own over the same
+// vector-to-thread map, each finishing thread loading the R partials of its
+// vector at once.  With RMSNorm the bf16 residual_out vectors stay in shared
+// memory for the second pass, and a split row combines its partial sums of
+// squares across the CTAs of a thread-block cluster through distributed
+// shared memory, as in the plain finalize.  The finishing threads, their
+// vectors, passes and warps are the same in every form of one plan, and so
+// is the order of the sum of squares: the forms' results are bit-identical.
 //
 // Launch order: a programmatic dependent of the previous kernel on the
 // stream (griddepcontrol.wait before any global memory access); it lets the
@@ -212,10 +212,10 @@ __device__ __forceinline__ void norm_tail(const ArParams &p, bool finisher, int 
 }
 
 // One rank per group (lanes = R): the one-shot call (every rank's rows) and
-// phase 1 (one rank, fp32 partial out), and, with p.reduce, phase 2 over the
-// ranks' fp32 partials for grids of at most one CTA per SM, where a thread
-// per rank and vector keeps the partials' loads spread over the CTA.  Every
-// group's partial of a pass meets group 0 in shared memory.
+// phase 1 (one rank, fp32 partial out), and, with p.reduce, phase 2 of the
+// same plans over the ranks' fp32 partials, a thread per rank and vector
+// keeping the partials' loads spread over the CTA.  Every group's partial of
+// a pass meets group 0 in shared memory.
 // PASSES: with RMSNorm, the number of passes over the slice (1, 2, 4 or 8),
 // fixed so that the gamma vectors can be held in registers; 0 without
 // RMSNorm (any number of passes).
@@ -454,9 +454,10 @@ finalize_ar_multi_kernel(const __grid_constant__ ArParams p) {
                                         s_part);
 }
 
-// Phase 2: the finishing threads of the plan alone (nvc rounded up to whole
-// warps), each loading the R fp32 partials of its vector at once and adding
-// them in rank order, then the epilogue.  No shared-memory exchange.
+// Phase 2 of plans with groups of several ranks: the plan's finishing
+// threads alone (nvc rounded up to whole warps), each loading the R fp32
+// partials of its vector at once and adding them in rank order, then the
+// epilogue.  No shared-memory exchange.
 template <int VEC, bool NORM, bool CLUSTER, int PASSES>
 __global__ void __launch_bounds__(kArMaxThreads, 1)
 finalize_ar_reduce_kernel(const __grid_constant__ ArParams p) {
@@ -563,8 +564,8 @@ cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms
                         cudaStream_t stream) {
     const int cluster = CLUSTER ? plan.cluster : 1;
     const bool small = plan.grid <= num_sms;
-    if (plan.lanes == p.ranks && (!p.reduce || small)) {
-        // one rank per group: gathering, or phase 2 of a small grid
+    if (plan.lanes == p.ranks) {
+        // one rank per group: gathering, or phase 2 in rank groups
         static std::atomic<int> big[2][64];
         if (small)
             return launch_ar_kernel(finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES, 1>, big[1], p,

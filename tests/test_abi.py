@@ -377,9 +377,9 @@ def test_allreduce_kernel_indices_stay_in_their_buffers(mf):
                                 assert q <= p["passes"]
                     if norm and p["cluster"] > 1:
                         assert p["cluster"] == p["splits"] <= min(16, threads)
-                    # phase 2 (grids above one CTA per SM, or groups of
-                    # several ranks): the nvc finishing threads alone, in whole
-                    # warps, with the kept vectors at the start of shared memory
+                    # phase 2 of plans with groups of several ranks: the nvc
+                    # finishing threads alone, in whole warps, with the kept
+                    # vectors at the start of shared memory
                     threads2 = -(-nvc // 32) * 32
                     assert threads2 <= 512 and (not norm or threads % 32 == 0)
                     for split in range(p["splits"]):
