@@ -458,8 +458,13 @@ finalize_ar_multi_kernel(const __grid_constant__ ArParams p) {
 // threads alone (nvc rounded up to whole warps), each loading the R fp32
 // partials of its vector at once and adding them in rank order, then the
 // epilogue.  No shared-memory exchange.
-template <int VEC, bool NORM, bool CLUSTER, int PASSES>
-__global__ void __launch_bounds__(kArMaxThreads, 1)
+// MINB: 1 (up to 128 registers: every partial's load in flight at once) for
+// grids that are resident all at once with that many registers; 2 (64
+// registers, the partials loaded 4 at a time) for larger grids, which then
+// fit twice as many CTAs per SM (R = 8, T = 256: 512 CTAs of 224 threads in
+// one wave instead of two).
+template <int VEC, bool NORM, bool CLUSTER, int PASSES, int MINB>
+__global__ void __launch_bounds__(kArMaxThreads, MINB)
 finalize_ar_reduce_kernel(const __grid_constant__ ArParams p) {
     using Ops = VecOps<VEC>;
     using FOps = F32Ops<VEC>;
@@ -495,16 +500,25 @@ finalize_ar_reduce_kernel(const __grid_constant__ ArParams p) {
             V rs{};
             if constexpr (NORM) rs = Ops::load(p.residual + at);
             float acc[VEC];
-            float f[MOEF_MAX_RANKS - 1][VEC];
             FOps::load(p.partial[0] + at, acc);
+            // the other ranks' partials in batches of kBatch loads in flight
+            // (all at once with the registers of the small-grid build)
+            constexpr int kBatch = MINB == 1 ? MOEF_MAX_RANKS - 1 : 4;
 #pragma unroll
-            for (int rr = 1; rr < MOEF_MAX_RANKS; ++rr)
-                if (rr < R) FOps::load(p.partial[rr] + at, f[rr - 1]);
+            for (int b0 = 1; b0 < MOEF_MAX_RANKS; b0 += kBatch) {
+                float f[kBatch][VEC];
 #pragma unroll
-            for (int rr = 1; rr < MOEF_MAX_RANKS; ++rr) {
-                if (rr < R) {
+                for (int i = 0; i < kBatch; ++i) {
+                    const int rr = b0 + i;
+                    if (rr < MOEF_MAX_RANKS && rr < R) FOps::load(p.partial[rr] + at, f[i]);
+                }
 #pragma unroll
-                    for (int c = 0; c < VEC; ++c) acc[c] += f[rr - 1][c];
+                for (int i = 0; i < kBatch; ++i) {
+                    const int rr = b0 + i;
+                    if (rr < MOEF_MAX_RANKS && rr < R) {
+#pragma unroll
+                        for (int c = 0; c < VEC; ++c) acc[c] += f[i][c];
+                    }
                 }
             }
             finish_vector<VEC, NORM>(p, at, acc, rs, s_keep + q * nvc + j, ss);
@@ -574,12 +588,16 @@ cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms
                                 plan.grid, plan.threads, plan.smem_bytes, cluster, stream);
     }
     if (p.reduce) {
-        static std::atomic<int> big[64];
+        static std::atomic<int> big[2][64];
         const int threads = (plan.nvc + 31) / 32 * 32;
         const int smem =
             NORM ? PASSES * plan.nvc * static_cast<int>(sizeof(typename VecOps<VEC>::V)) : 0;
-        return launch_ar_kernel(finalize_ar_reduce_kernel<VEC, NORM, CLUSTER, PASSES>, big, p,
-                                plan.grid, threads, smem, cluster, stream);
+        const int64_t resident = static_cast<int64_t>(num_sms) * (65536 / (threads * 128));
+        if (plan.grid <= resident)
+            return launch_ar_kernel(finalize_ar_reduce_kernel<VEC, NORM, CLUSTER, PASSES, 1>,
+                                    big[1], p, plan.grid, threads, smem, cluster, stream);
+        return launch_ar_kernel(finalize_ar_reduce_kernel<VEC, NORM, CLUSTER, PASSES, 2>, big[0],
+                                p, plan.grid, threads, smem, cluster, stream);
     }
     // groups of several ranks: planned for 16-byte vectors only
     if constexpr (VEC == 8) {
