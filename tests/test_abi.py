@@ -324,6 +324,23 @@ def test_allreduce_plans(mf):
         mf.allreduce_plan(9, 1, 7168, True)
 
 
+def test_allreduce_parity_shapes_cover_every_layout(mf):
+    """The all-reduce parity cases run every kernel layout the planner can
+    pick: one rank per thread group, rank pairs and one thread summing all
+    ranks, each with and without RMSNorm, and the scalar (unaligned-H) path."""
+    from test_allreduce import CASES
+    seen = set()
+    for R, T, K, H, wkind, norm in CASES:
+        p = mf.allreduce_plan(R, T, H, norm)
+        layout = ("scalar" if p["vec"] == 1 else
+                  "one rank per group" if p["lanes"] == R else
+                  "all ranks" if p["lanes"] == 1 else "rank pairs")
+        seen.add((layout, norm))
+    want = {(lay, norm) for lay in ("one rank per group", "rank pairs", "all ranks")
+            for norm in (False, True)} | {("scalar", True)}
+    assert want <= seen, want - seen
+
+
 def test_allreduce_kernel_indices_stay_in_their_buffers(mf):
     """The all-reduce kernel's index arithmetic, replayed on the host for
     every plan of the decode, test and benchmark shapes: each thread's rank

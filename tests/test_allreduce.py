@@ -100,6 +100,13 @@ CASES = [
     (7, 33, 5, 5120, "fp32", False),
     (3, 5, 2, 64, "fp32", True),         # a row shorter than a warp per rank: padded to whole warps
     (5, 2, 3, 40, "bf16", True),         # scalar path, 5 ranks, 40 values a row
+    (6, 16, 8, 7168, "fp32", True),      # 3 groups of rank pairs
+    (6, 12, 8, 7168, "bf16", False),     # rank pairs, no residual
+    (8, 20, 4, 4104, "fp32", True),      # rank pairs over a ragged row
+    (6, 64, 8, 7168, "packed", True),    # one thread sums 6 ranks
+    (3, 70, 4, 4104, "fp32", True),      # one thread sums 3 ranks, ragged row
+    (2, 100, 8, 2048, "bf16", False),    # one thread sums 2 ranks, no residual
+    (7, 16, 8, 7168, "fp32", True),      # odd R: one rank per group from 5 tokens on
 ]
 
 
