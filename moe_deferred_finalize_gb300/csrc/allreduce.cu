@@ -25,15 +25,17 @@
 // (g, j) obtains its ranks' partials of vector j of the CTA's slice one
 // after another (per rank K gathered-row loads, 16 bytes each, plus the
 // shared-output load), so a pass keeps `lanes` times as many loads in flight
-// as one thread summing all ranks would.  The partials meet group 0 in
-// shared memory, where it adds them in rank order and finishes the vector.
+// as one thread summing all ranks would.  Group 0 adds its own ranks'
+// partials in registers and the other groups' from shared memory, in rank
+// order, and finishes the vector.
 // Decode sizes use lanes = R (or R / 2 from 5 tokens on when R > 4); with
 // many tokens, enough vectors to fill the GPU, lanes = 1: each thread sums
 // all ranks itself, with no exchange or barrier per pass.  Phase 2 of a
 // one-rank-per-group plan runs in the same groups over the fp32 partials;
 // phase 2 of the other plans runs a kernel of its own over the same
 // vector-to-thread map, each finishing thread loading the R partials of its
-// vector at once.  With RMSNorm the bf16 residual_out vectors stay in shared
+// vector itself (all at once, or four at a time for grids too large to be
+// resident at once).  With RMSNorm the bf16 residual_out vectors stay in shared
 // memory for the second pass, and a split row combines its partial sums of
 // squares across the CTAs of a thread-block cluster through distributed
 // shared memory, as in the plain finalize.  The finishing threads, their
