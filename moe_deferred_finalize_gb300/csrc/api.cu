@@ -418,7 +418,11 @@ int pow2_bucket(int need) {
 //    Each extra pass over a slice costs a full chain of loads, barrier and
 //    epilogue (about 2.8 us at R = 8, T = 1), so a few tokens take CTAs of
 //    up to 512 threads (`lanes` groups of 512 / lanes, at most 256), enough for one
-//    pass: with R = 8 at H = 7168, 14 CTAs of 8 x 64 threads.  From T = 5 on
+//    pass, and with R > 1 a split row over a full cluster of 16 (slices of
+//    at least 32 vectors), so that more SMs share the ranks' rows: with R =
+//    8 at H = 7168, 16 CTAs of 8 x 64 threads (T = 1: 4.28 -> 4.24 us
+//    against 14 CTAs; R = 2: 4.19 -> 3.91 us against 4 CTAs of 2 x 224
+//    threads; R = 4: 4.31 -> 4.04 us; H = 4096: 0.05-0.24 us faster).  From T = 5 on
 //    CTAs of 256 threads win even with a second pass (R = 4, T = 16: 14 x
 //    256 threads 5.6 us vs 7 x 512 threads 9.3 us; R = 8: 16 x 224 threads
 //    9.2 us vs 14 x 512 threads 11.9 us).  The split is halved while the grid
@@ -492,6 +496,15 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
             if (nvc_max > 256) nvc_max = 256;
             nvc_max = nvc_max / 32 * 32;
             splits = ceil_div(nvec, nvc_max);
+            // a few tokens over several ranks, a row already split: the row
+            // over a full cluster (slices of at least 32 vectors), so that
+            // more SMs share the ranks' rows.  A row that fits one CTA stays
+            // there: a cluster's barrier costs more than it gains (R = 2,
+            // H = 2048: 3.23 us in one CTA, 3.63 us over 8)
+            if (T <= 4 && R > 1 && splits > 1 && splits < kMaxCluster) {
+                const int wide = nvec / 32 < kMaxCluster ? nvec / 32 : kMaxCluster;
+                if (wide > splits) splits = wide;
+            }
             if (splits > kMaxCluster) splits = kMaxCluster;
             if (ceil_div(ceil_div(nvec, splits), nvc_max) > kArMaxPasses) return MOEF_ERR_SHAPE;
             while (splits > 1 && rows * splits > 4 * static_cast<int64_t>(num_sms)) {

@@ -312,7 +312,11 @@ def test_allreduce_plans(mf):
                         assert p["smem_bytes"] <= 48 * 1024
     # the decode shapes: every rank's loads of a vector in flight in one pass
     p = mf.allreduce_plan(8, 1, 7168, True)
-    assert (p["nvc"], p["splits"], p["passes"], p["cluster"]) == (64, 14, 1, 14)
+    assert (p["nvc"], p["splits"], p["passes"], p["cluster"]) == (64, 16, 1, 16)
+    p = mf.allreduce_plan(2, 1, 7168, True)           # a split row widened to 16 CTAs
+    assert (p["nvc"], p["splits"], p["cluster"]) == (64, 16, 16)
+    p = mf.allreduce_plan(2, 1, 2048, True)           # a row that fits one CTA stays there
+    assert (p["splits"], p["cluster"]) == (1, 1)
     # many tokens: one thread per vector summing the 8 ranks, rows in 2
     # slices of 2 passes over 224 vectors
     p = mf.allreduce_plan(8, 256, 7168, True)
