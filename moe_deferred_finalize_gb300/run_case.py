@@ -7,8 +7,15 @@ For profilers: one process, a handful of launches, a known input size.
   python -m moe_deferred_finalize_gb300.run_case --workload decode_bs1_packed --unfused
   python -m moe_deferred_finalize_gb300.run_case --gate-tokens 16384 --iters 3
   python -m moe_deferred_finalize_gb300.run_case --tp 8 16 --form one_shot --iters 3
+  python -m moe_deferred_finalize_gb300.run_case --tp-procs 16 --iters 300
+
+--tp-procs times the orchestration of the all-reduce-fused finalize across
+processes (moe_deferred_finalize_gb300.tp, two-phase form): two processes on
+GPU 0, a gloo group for set-up and the per-step host barrier; it prints the
+wall time per step and of the barrier alone.
 """
 import argparse
+import time
 
 import numpy as np
 import torch
@@ -24,6 +31,63 @@ def _dev(a):
     return torch.from_numpy(a).cuda()
 
 
+def _tp_procs_worker(rank, port, T, steps, q):
+    import torch.distributed as dist
+    from moe_deferred_finalize_gb300 import tp
+    torch.cuda.set_device(0)
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=2)
+    try:
+        g = W.tp_decode(2, T, seed=7)
+        wl = g.ranks[rank]
+        x = {"permuted_out": _dev(wl.permuted_out), "idx_map": _dev(wl.idx),
+             "weights": _dev(wl.weights), "shared_out": _dev(wl.shared)}
+        outs = {k: torch.empty((T, g.H), dtype=torch.bfloat16, device="cuda")
+                for k in ("out", "residual_out", "norm_out")}
+        ep = dict(residual=_dev(g.residual), gamma=_dev(g.gamma), eps=g.eps)
+        group = tp.TPFinalize(dist.group.WORLD, T, g.H)
+        res = {}
+        for n, key in ((20, None), (steps, "us_per_step")):
+            torch.cuda.synchronize()
+            dist.barrier()
+            t0 = time.perf_counter()
+            for _ in range(n):
+                group.step(x, g.wkind, g.routed_scale, T, outs=outs, **ep)
+            torch.cuda.synchronize()
+            if key:
+                res[key] = (time.perf_counter() - t0) / n * 1e6
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            dist.barrier()
+        res["us_per_barrier"] = (time.perf_counter() - t0) / steps * 1e6
+        group.close()
+        q.put((rank, res))
+    finally:
+        dist.destroy_process_group()
+
+
+def _tp_procs(T, steps):
+    import multiprocessing as mp
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_tp_procs_worker, args=(r, port, T, steps, q)) for r in range(2)]
+    for pr in procs:
+        pr.start()
+    got = dict(q.get(timeout=600) for _ in procs)
+    for pr in procs:
+        pr.join(120)
+        if pr.exitcode != 0:
+            raise RuntimeError(f"rank process exited with {pr.exitcode}")
+    for rank in sorted(got):
+        r = got[rank]
+        print(f"tp-procs: rank {rank} T={T} steps={steps}: {r['us_per_step']:.1f} us per "
+              f"two-phase step, {r['us_per_barrier']:.1f} us per host barrier")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     g = ap.add_mutually_exclusive_group(required=True)
@@ -34,6 +98,9 @@ def main(argv=None):
     g.add_argument("--tp", type=int, nargs=2, metavar=("R", "T"),
                    help="the all-reduce-fused finalize over R ranks at decode batch T "
                         "(1, 16 or 256), H=7168, residual + RMSNorm")
+    g.add_argument("--tp-procs", type=int, metavar="T",
+                   help="time the two-process orchestration (two-phase form, R=2) at batch T "
+                        "(1, 16 or 256) on GPU 0 for --iters steps")
     ap.add_argument("--form", choices=["one_shot", "two_phase", "plain"], default="one_shot",
                     help="with --tp: one-shot, two-phase (phase 1 per rank, then phase 2), "
                          "or the plain finalize of rank 0's operands")
@@ -44,6 +111,9 @@ def main(argv=None):
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--threads", type=int, default=0)
     args = ap.parse_args(argv)
+    if args.tp_procs:
+        _tp_procs(args.tp_procs, args.iters)
+        return
     if args.gate_tokens:
         g_ = torch.Generator(device="cuda").manual_seed(0)
         z = torch.randn((args.gate_tokens, 256), generator=g_, device="cuda")
