@@ -28,9 +28,10 @@
 // as one thread summing all ranks would.  Group 0 adds its own ranks'
 // partials in registers and the other groups' from shared memory, in rank
 // order, and finishes the vector.
-// Decode sizes use lanes = R (or R / 2 from 5 tokens on when R > 4); with
-// many tokens, enough vectors to fill the GPU, lanes = 1: each thread sums
-// all ranks itself, with no exchange or barrier per pass.  Phase 2 of a
+// Decode sizes use lanes = R (or R / 2 from 5 tokens on when R > 4, and 2
+// from 44 tokens on when R >= 6); with many tokens, enough vectors to fill
+// the GPU, lanes = 1: each thread sums all ranks itself, with no exchange or
+// barrier per pass.  Phase 2 of a
 // one-rank-per-group plan runs in the same groups over the fp32 partials;
 // phase 2 of the other plans runs a kernel of its own over the same
 // vector-to-thread map, each finishing thread loading the R partials of its
@@ -346,11 +347,12 @@ finalize_ar_kernel(const __grid_constant__ ArParams p) {
 }
 
 // Groups of several ranks, gathering only (one-shot), 16-byte vectors:
-// MODE kRankPairs (lanes = R / 2: group g sums ranks 2g and 2g + 1 one after
-// the other; groups other than 0 store each rank's partial, and group 0 adds
-// ranks 2 .. R-1 from shared memory in rank order) or kAllRanks (lanes = 1:
-// each thread sums every rank's partial in rank order itself, no exchange).
-enum { kRankPairs = 1, kAllRanks = 2 };
+// MODE kRankGroups (1 < lanes < R: group g sums its c = R / lanes ranks
+// g*c .. g*c + c - 1 one after the other; groups other than 0 store each
+// rank's partial, and group 0 adds ranks c .. R-1 from shared memory in rank
+// order) or kAllRanks (lanes = 1: each thread sums every rank's partial in
+// rank order itself, no exchange).
+enum { kRankGroups = 1, kAllRanks = 2 };
 
 template <int VEC, bool NORM, bool CLUSTER, int PASSES, int MODE>
 __global__ void __launch_bounds__(kArMaxThreads, 2)
@@ -365,18 +367,18 @@ finalize_ar_multi_kernel(const __grid_constant__ ArParams p) {
     __shared__ float s_part[kArMaxCluster];
     const int nvc = p.nvc;
     const int R = p.ranks;
-    // ranks per group: 2 for pairs, taken as a run-time count (measured
-    // faster in this kernel than the constant), or all R
-    const int c = MODE == kRankPairs ? R / p.lanes : R;
-    // dynamic: pairs: the partials of ranks 2 .. R-1 for one pass, float
-    // [R - 2][nvc][VEC]; then with RMSNorm the kept residual_out vectors, V [PASSES][nvc]
+    // ranks per group: R / lanes (2 or R / 2), a run-time count (measured
+    // faster in this kernel than a constant 2 for pairs), or all R
+    const int c = MODE == kRankGroups ? R / p.lanes : R;
+    // dynamic: the partials of ranks c .. R-1 for one pass, float
+    // [R - c][nvc][VEC]; then with RMSNorm the kept residual_out vectors, V [PASSES][nvc]
     extern __shared__ __align__(16) unsigned char s_dyn[];
     float *s_p = reinterpret_cast<float *>(s_dyn);
     V *s_keep = reinterpret_cast<V *>(s_dyn + sizeof(float) * VEC * (R - c) * nvc);
 
     if constexpr (CLUSTER) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
-    const int g = MODE == kRankPairs ? threadIdx.x / nvc : 0;   // this thread's group
+    const int g = MODE == kRankGroups ? threadIdx.x / nvc : 0;   // this thread's group
     const int j = threadIdx.x - g * nvc;                        // its vector within a pass
     const int r0 = g * c;                                       // the group's first rank
     const int S = p.splits;
@@ -432,7 +434,7 @@ finalize_ar_multi_kernel(const __grid_constant__ ArParams p) {
                 }
             }
         }
-        if constexpr (MODE == kRankPairs) {
+        if constexpr (MODE == kRankGroups) {
             __syncthreads();
             if (g == 0 && active) {
                 for (int rr = c; rr < R; ++rr) {
@@ -608,8 +610,8 @@ cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms
             return launch_ar_kernel(finalize_ar_multi_kernel<VEC, NORM, CLUSTER, PASSES, kAllRanks>,
                                     big[1], p, plan.grid, plan.threads, plan.smem_bytes, cluster,
                                     stream);
-        if (p.ranks == 2 * plan.lanes)
-            return launch_ar_kernel(finalize_ar_multi_kernel<VEC, NORM, CLUSTER, PASSES, kRankPairs>,
+        if (p.ranks % plan.lanes == 0)
+            return launch_ar_kernel(finalize_ar_multi_kernel<VEC, NORM, CLUSTER, PASSES, kRankGroups>,
                                     big[0], p, plan.grid, plan.threads, plan.smem_bytes, cluster,
                                     stream);
     }

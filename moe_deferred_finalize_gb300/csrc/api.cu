@@ -396,6 +396,13 @@ constexpr int kArSeqSlice = MOEF_AR_SEQ_SLICE;
 #ifndef MOEF_AR_SEQ_MAX_THREADS
 #define MOEF_AR_SEQ_MAX_THREADS 256
 #endif
+// Tokens from which R >= 6 ranks (even) go in two groups of R / 2, up to
+// the sequential-ranks plans: where groups of two ranks would need a second
+// pass over the slice (the split halved past 4 CTAs per SM).
+#ifndef MOEF_AR_HALVES_MIN_TOKENS
+#define MOEF_AR_HALVES_MIN_TOKENS 44
+#endif
+constexpr int kArHalvesMinTokens = MOEF_AR_HALVES_MIN_TOKENS;
 constexpr int kArMidLanes = MOEF_AR_MID_LANES;
 constexpr int kArSeqMaxThreads = MOEF_AR_SEQ_MAX_THREADS;
 
@@ -427,6 +434,13 @@ int pow2_bucket(int need) {
 //    256 threads 5.6 us vs 7 x 512 threads 9.3 us; R = 8: 16 x 224 threads
 //    9.2 us vs 14 x 512 threads 11.9 us).  The split is halved while the grid
 //    exceeds 4 CTAs per SM, each thread then taking up to 8 passes.
+// From kArHalvesMinTokens on, R >= 6 ranks (even) go in two groups of R / 2
+// (CTAs of 2 x 128 threads, one pass), where rank pairs would need a second
+// pass: R = 8, T = 48: 15.3 / 8.2 us against 16.7 / 9.4 us (one-shot /
+// two-phase per rank); R = 6: 12.8 / 7.8 against 14.4 / 8.8.  Up to T = 80
+// the one-shot keeps gaining (R = 8, T = 64: 17.1 against 18.6 us), but the
+// two-phase form, the faster one there, loses (9.2 against 8.8 us), so the
+// sequential plans take over at kArSeqMinTokens.
 // With many tokens (R > 1, T >= kArSeqMinTokens, 16-byte vectors) the
 // tokens alone fill the GPU, and each thread sums the ranks of its vector in
 // sequence (lanes = 1).  Slices start at kArSeqSlice vectors, one pass each;
@@ -447,7 +461,9 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
     const int nvec = H / vec;
     const int64_t rows = T > 0 ? T : 1;
     int lanes = R, nvc = 0, splits = 0, slice = 0, passes = 0;
-    if (R > 1 && vec == 8 && T >= kArSeqMinTokens) {
+    const bool halves = R >= 6 && R % 2 == 0 && vec == 8 && T >= kArHalvesMinTokens &&
+                        T < kArSeqMinTokens;
+    if (R > 1 && vec == 8 && T >= kArSeqMinTokens && !halves) {
         lanes = 1;
         if (!with_norm) {
             nvc = kArSeqSlice < nvec ? kArSeqSlice : nvec;
@@ -478,7 +494,8 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
         }
     }
     if (lanes > 1 || R == 1) {
-        if (T > 4 && R > kArMidLanes && R % 2 == 0 && vec == 8) lanes = R / 2;
+        if (halves) lanes = 2;
+        else if (T > 4 && R > kArMidLanes && R % 2 == 0 && vec == 8) lanes = R / 2;
         if (!with_norm) {
             nvc = 128 / lanes / 16 * 16;
             if (nvc < 16) nvc = 16;
@@ -530,7 +547,7 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
     const int vbytes = vec == 8 ? 16 : 2;
     // the exchanged partials of a pass: every group's with one rank per group,
     // ranks 2 .. R-1 with pairs, none when one thread sums all ranks
-    const int exchanged = lanes == R ? (lanes > 1 ? R : 0) : lanes > 1 ? R - 2 : 0;
+    const int exchanged = lanes == R ? (lanes > 1 ? R : 0) : lanes > 1 ? R - R / lanes : 0;
     int64_t smem = static_cast<int64_t>(sizeof(float)) * vec * exchanged * nvc +
                    (with_norm ? static_cast<int64_t>(passes) * nvc * vbytes : 0);
     plan->vec = vec;

@@ -282,7 +282,7 @@ def test_allreduce_plans(mf):
     and at most 8 passes per thread."""
     for R in range(1, 9):
         for H in (8, 64, 100, 1000, 2048, 4104, 7168, 16384, 65536):
-            for T in (1, 16, 256, 4096):
+            for T in (1, 16, 48, 64, 256, 4096):
                 for norm in (False, True):
                     for vec_ok in (True, False):
                         try:
@@ -293,8 +293,10 @@ def test_allreduce_plans(mf):
                         nvec = H // p["vec"]
                         # rank groups at decode sizes; each thread summing the
                         # ranks in sequence once the tokens fill the GPU
-                        seq = R > 1 and p["vec"] == 8 and T >= 64
-                        mid = R // 2 if T > 4 and R > 4 and R % 2 == 0 and p["vec"] == 8 else R
+                        halves = R >= 6 and R % 2 == 0 and p["vec"] == 8 and 44 <= T < 64
+                        seq = R > 1 and p["vec"] == 8 and T >= 64 and not halves
+                        mid = (2 if halves else
+                               R // 2 if T > 4 and R > 4 and R % 2 == 0 and p["vec"] == 8 else R)
                         if seq and norm and p["lanes"] == mid:
                             assert -(-nvec // 16) > 8 * 512      # row too long for one
                         else:
@@ -338,10 +340,11 @@ def test_allreduce_parity_shapes_cover_every_layout(mf):
         p = mf.allreduce_plan(R, T, H, norm)
         layout = ("scalar" if p["vec"] == 1 else
                   "one rank per group" if p["lanes"] == R else
-                  "all ranks" if p["lanes"] == 1 else "rank pairs")
+                  "all ranks" if p["lanes"] == 1 else
+                  "rank pairs" if 2 * p["lanes"] == R else "two rank groups")
         seen.add((layout, norm))
     want = {(lay, norm) for lay in ("one rank per group", "rank pairs", "all ranks")
-            for norm in (False, True)} | {("scalar", True)}
+            for norm in (False, True)} | {("scalar", True), ("two rank groups", True)}
     assert want <= seen, want - seen
 
 
@@ -352,7 +355,7 @@ def test_allreduce_kernel_indices_stay_in_their_buffers(mf):
     pass, the kept residual_out vectors), the slot staging and the cluster
     pushes all stay inside what the plan allocates."""
     for R in range(1, 9):
-        for T in (1, 4, 5, 16, 256, 1024):
+        for T in (1, 4, 5, 16, 48, 64, 256, 1024):
             for H in (64, 100, 512, 1000, 2048, 4096, 4104, 5120, 7168, 16384):
                 for norm in (False, True):
                     try:
@@ -363,15 +366,15 @@ def test_allreduce_kernel_indices_stay_in_their_buffers(mf):
                     nvec = H // vec
                     vbytes = 16 if vec == 8 else 2
                     c = R // lanes                      # ranks per group
-                    assert c * lanes == R and (c == 1 or vec == 8) and c in (1, 2, R)
+                    assert c * lanes == R and (c == 1 or vec == 8)
                     # exchanged partials of a pass: every group's (one rank per
-                    # group), ranks 2 .. R-1 (pairs), none (one thread, all ranks)
-                    sp_bytes = 4 * vec * (R if 1 < lanes == R else R - 2 if c == 2 and lanes > 1
-                                          else 0) * nvc
+                    # group), ranks c .. R-1 (groups of c ranks), none (one
+                    # thread summing all ranks)
+                    sp_bytes = 4 * vec * (R if 1 < lanes == R else R - c if lanes > 1 else 0) * nvc
                     keep_bytes = p["passes"] * nvc * vbytes if norm else 0
                     assert sp_bytes + keep_bytes == p["smem_bytes"]
                     assert threads <= 512 and threads // 32 <= 16 and R * 32 <= 256
-                    assert lanes in (1, R, R // 2)
+                    assert lanes in (1, 2, R, R // 2)
                     for split in range(p["splits"]):
                         v_begin = split * p["slice"]
                         v_end = min(v_begin + p["slice"], nvec)
@@ -382,9 +385,9 @@ def test_allreduce_kernel_indices_stay_in_their_buffers(mf):
                                 assert rr < R
                                 if lanes == R > 1:    # partial word (rr, j, .) of a pass
                                     assert (rr * nvc + j + 1) * vec * 4 <= sp_bytes
-                                elif g > 0:           # pairs: word (rr - 2, j, .)
-                                    assert 0 <= (rr - 2) * nvc + j and \
-                                        ((rr - 2) * nvc + j + 1) * vec * 4 <= sp_bytes
+                                elif g > 0:           # groups of c: word (rr - c, j, .)
+                                    assert 0 <= (rr - c) * nvc + j and \
+                                        ((rr - c) * nvc + j + 1) * vec * 4 <= sp_bytes
                             q = 0
                             for base in range(v_begin, v_end, nvc):
                                 v = base + j
