@@ -396,13 +396,6 @@ constexpr int kArSeqSlice = MOEF_AR_SEQ_SLICE;
 #ifndef MOEF_AR_SEQ_MAX_THREADS
 #define MOEF_AR_SEQ_MAX_THREADS 256
 #endif
-// Tokens from which R >= 6 ranks (even) go in two groups of R / 2, up to
-// the sequential-ranks plans: where groups of two ranks would need a second
-// pass over the slice (the split halved past 4 CTAs per SM).
-#ifndef MOEF_AR_HALVES_MIN_TOKENS
-#define MOEF_AR_HALVES_MIN_TOKENS 44
-#endif
-constexpr int kArHalvesMinTokens = MOEF_AR_HALVES_MIN_TOKENS;
 constexpr int kArMidLanes = MOEF_AR_MID_LANES;
 constexpr int kArSeqMaxThreads = MOEF_AR_SEQ_MAX_THREADS;
 
@@ -434,13 +427,19 @@ int pow2_bucket(int need) {
 //    256 threads 5.6 us vs 7 x 512 threads 9.3 us; R = 8: 16 x 224 threads
 //    9.2 us vs 14 x 512 threads 11.9 us).  The split is halved while the grid
 //    exceeds 4 CTAs per SM, each thread then taking up to 8 passes.
-// From kArHalvesMinTokens on, R >= 6 ranks (even) go in two groups of R / 2
-// (CTAs of 2 x 128 threads, one pass), where rank pairs would need a second
-// pass: R = 8, T = 48: 15.3 / 8.2 us against 16.7 / 9.4 us (one-shot /
-// two-phase per rank); R = 6: 12.8 / 7.8 against 14.4 / 8.8.  Up to T = 80
-// the one-shot keeps gaining (R = 8, T = 64: 17.1 against 18.6 us), but the
-// two-phase form, the faster one there, loses (9.2 against 8.8 us), so the
-// sequential plans take over at kArSeqMinTokens.
+// From 5 tokens up to the sequential-ranks plans, R >= 4 ranks (even) go in
+// two groups of R / 2 (CTAs of 2 x 128 threads) once the plan above would
+// not have all its rows' clusters resident at once, or would need a second
+// pass.  14-CTA clusters of 256-thread CTAs fit about 35 at a time: R = 8,
+// T = 36: 13.3 us against 17.6 us one-shot; R = 4, T = 36: 8.7 / 7.0
+// against 11.2 / 10.0 us (one-shot / two-phase per rank).  192-thread CTAs
+// (R = 6 pairs) fit about 43, so R = 6 keeps its pairs up to T = 43 (T = 40:
+// 10.9 against 11.9 us one-shot).  Past 4 CTAs per SM pairs would take a
+// second pass: R = 8, T = 48: 15.3 / 8.2 us against 16.7 / 9.4 us; R = 6:
+// 12.8 / 7.8 against 14.4 / 8.8.  Up to T = 80 the one-shot keeps gaining
+// (R = 8, T = 64: 17.1 against 18.6 us), but the two-phase form, the faster
+// one there, loses (9.2 against 8.8 us), so the sequential plans take over
+// at kArSeqMinTokens.
 // With many tokens (R > 1, T >= kArSeqMinTokens, 16-byte vectors) the
 // tokens alone fill the GPU, and each thread sums the ranks of its vector in
 // sequence (lanes = 1).  Slices start at kArSeqSlice vectors, one pass each;
@@ -461,9 +460,7 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
     const int nvec = H / vec;
     const int64_t rows = T > 0 ? T : 1;
     int lanes = R, nvc = 0, splits = 0, slice = 0, passes = 0;
-    const bool halves = R >= 6 && R % 2 == 0 && vec == 8 && T >= kArHalvesMinTokens &&
-                        T < kArSeqMinTokens;
-    if (R > 1 && vec == 8 && T >= kArSeqMinTokens && !halves) {
+    if (R > 1 && vec == 8 && T >= kArSeqMinTokens) {
         lanes = 1;
         if (!with_norm) {
             nvc = kArSeqSlice < nvec ? kArSeqSlice : nvec;
@@ -493,47 +490,76 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
             }
         }
     }
-    if (lanes > 1 || R == 1) {
-        if (halves) lanes = 2;
-        else if (T > 4 && R > kArMidLanes && R % 2 == 0 && vec == 8) lanes = R / 2;
+    // the plan of `ln` groups of threads (ln > 1, or R = 1)
+    auto group_plan = [&](int ln, int *nvc_o, int *splits_o, int *slice_o,
+                          int *passes_o) -> moef_status {
+        int nv, sp, sl, pa;
         if (!with_norm) {
-            nvc = 128 / lanes / 16 * 16;
-            if (nvc < 16) nvc = 16;
-            if (nvc > nvec) nvc = nvec;
-            slice = nvc;
-            splits = ceil_div(nvec, slice);
-            if (rows * splits > 0x7FFFFFFFLL) {
-                splits = static_cast<int>(0x7FFFFFFFLL / rows);
-                if (splits < 1) splits = 1;
-                slice = ceil_div(nvec, splits);
+            nv = 128 / ln / 16 * 16;
+            if (nv < 16) nv = 16;
+            if (nv > nvec) nv = nvec;
+            sl = nv;
+            sp = ceil_div(nvec, sl);
+            if (rows * sp > 0x7FFFFFFFLL) {
+                sp = static_cast<int>(0x7FFFFFFFLL / rows);
+                if (sp < 1) sp = 1;
+                sl = ceil_div(nvec, sp);
             }
-            passes = ceil_div(slice, nvc);
+            pa = ceil_div(sl, nv);
         } else {
-            int nvc_max = (T <= 4 ? kArMaxThreads : kArMaxThreads / 2) / lanes;
+            int nvc_max = (T <= 4 ? kArMaxThreads : kArMaxThreads / 2) / ln;
             if (nvc_max > 256) nvc_max = 256;
             nvc_max = nvc_max / 32 * 32;
-            splits = ceil_div(nvec, nvc_max);
+            sp = ceil_div(nvec, nvc_max);
             // a few tokens over several ranks, a row already split: the row
             // over a full cluster (slices of at least 32 vectors), so that
             // more SMs share the ranks' rows.  A row that fits one CTA stays
             // there: a cluster's barrier costs more than it gains (R = 2,
             // H = 2048: 3.23 us in one CTA, 3.63 us over 8)
-            if (T <= 4 && R > 1 && splits > 1 && splits < kMaxCluster) {
+            if (T <= 4 && R > 1 && sp > 1 && sp < kMaxCluster) {
                 const int wide = nvec / 32 < kMaxCluster ? nvec / 32 : kMaxCluster;
-                if (wide > splits) splits = wide;
+                if (wide > sp) sp = wide;
             }
-            if (splits > kMaxCluster) splits = kMaxCluster;
-            if (ceil_div(ceil_div(nvec, splits), nvc_max) > kArMaxPasses) return MOEF_ERR_SHAPE;
-            while (splits > 1 && rows * splits > 4 * static_cast<int64_t>(num_sms)) {
-                const int half = ceil_div(splits, 2);
+            if (sp > kMaxCluster) sp = kMaxCluster;
+            if (ceil_div(ceil_div(nvec, sp), nvc_max) > kArMaxPasses) return MOEF_ERR_SHAPE;
+            while (sp > 1 && rows * sp > 4 * static_cast<int64_t>(num_sms)) {
+                const int half = ceil_div(sp, 2);
                 if (ceil_div(ceil_div(nvec, half), nvc_max) > kArMaxPasses) break;
-                splits = half;
+                sp = half;
             }
-            slice = ceil_div(nvec, splits);
-            passes = pow2_bucket(ceil_div(slice, nvc_max));
-            nvc = ceil_div(slice, passes);
-            if (nvc > 32) nvc = round_up(nvc, 32);
-            if (nvc > nvc_max) nvc = nvc_max;
+            sl = ceil_div(nvec, sp);
+            pa = pow2_bucket(ceil_div(sl, nvc_max));
+            nv = ceil_div(sl, pa);
+            if (nv > 32) nv = round_up(nv, 32);
+            if (nv > nvc_max) nv = nvc_max;
+        }
+        *nvc_o = nv;
+        *splits_o = sp;
+        *slice_o = sl;
+        *passes_o = pa;
+        return MOEF_OK;
+    };
+    if (lanes > 1 || R == 1) {
+        if (T > 4 && R > kArMidLanes && R % 2 == 0 && vec == 8) lanes = R / 2;
+        moef_status st = group_plan(lanes, &nvc, &splits, &slice, &passes);
+        if (st != MOEF_OK) return st;
+        // Two groups of R / 2 ranks instead, when the rows' clusters would
+        // not all be resident at once (CTAs of 64 registers a thread, about
+        // 4/5 of the SMs' room usable by clusters, as measured with
+        // launch__cluster_max_active) or would need a second pass
+        if (with_norm && R >= 4 && R % 2 == 0 && vec == 8 && T > 4 && lanes > 2 && splits > 1) {
+            const int64_t per_sm = 1024 / (static_cast<int64_t>(lanes) * nvc);
+            const int64_t fit = static_cast<int64_t>(num_sms) * per_sm * 4 / 5 / splits;
+            if (T > fit || passes > 1) {
+                int nv2, sp2, sl2, pa2;
+                if (group_plan(2, &nv2, &sp2, &sl2, &pa2) == MOEF_OK && pa2 <= passes) {
+                    lanes = 2;
+                    nvc = nv2;
+                    splits = sp2;
+                    slice = sl2;
+                    passes = pa2;
+                }
+            }
         }
     }
     // whole warps (the RMSNorm epilogue reduces with full-warp shuffles):

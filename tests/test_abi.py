@@ -293,14 +293,18 @@ def test_allreduce_plans(mf):
                         nvec = H // p["vec"]
                         # rank groups at decode sizes; each thread summing the
                         # ranks in sequence once the tokens fill the GPU
-                        halves = R >= 6 and R % 2 == 0 and p["vec"] == 8 and 44 <= T < 64
-                        seq = R > 1 and p["vec"] == 8 and T >= 64 and not halves
-                        mid = (2 if halves else
-                               R // 2 if T > 4 and R > 4 and R % 2 == 0 and p["vec"] == 8 else R)
-                        if seq and norm and p["lanes"] == mid:
-                            assert -(-nvec // 16) > 8 * 512      # row too long for one
+                        seq = R > 1 and p["vec"] == 8 and T >= 64
+                        groups = {R}                      # the layouts this size may take
+                        if p["vec"] == 8 and T > 4 and R % 2 == 0:
+                            if R > 4:
+                                groups.add(R // 2)
+                            if R >= 4 and norm:
+                                groups.add(2)
+                        if seq and p["lanes"] != 1:
+                            assert norm and -(-nvec // 16) > 8 * 512   # row too long for one
+                            assert p["lanes"] in groups
                         else:
-                            assert p["lanes"] == (1 if seq else mid)
+                            assert p["lanes"] in ({1} if seq else groups)
                         assert p["threads"] == p["lanes"] * p["nvc"] <= 512
                         assert p["threads"] % 32 == 0          # whole warps: full-mask shuffles
                         assert p["splits"] * p["slice"] >= nvec > (p["splits"] - 1) * p["slice"]
@@ -319,6 +323,10 @@ def test_allreduce_plans(mf):
     assert (p["nvc"], p["splits"], p["cluster"]) == (64, 16, 16)
     p = mf.allreduce_plan(2, 1, 2048, True)           # a row that fits one CTA stays there
     assert (p["splits"], p["cluster"]) == (1, 1)
+    # rank groups switch to two halves where the rows' 14-CTA clusters would
+    # not all be resident at once (T > ~35 for 256-thread CTAs, ~43 for 192)
+    for R, T, lanes in ((8, 34, 4), (8, 35, 2), (4, 34, 4), (4, 35, 2), (6, 43, 3), (6, 44, 2)):
+        assert mf.allreduce_plan(R, T, 7168, True)["lanes"] == lanes, (R, T)
     # many tokens: one thread per vector summing the 8 ranks, rows in 2
     # slices of 2 passes over 224 vectors
     p = mf.allreduce_plan(8, 256, 7168, True)

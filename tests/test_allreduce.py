@@ -108,7 +108,7 @@ CASES = [
     (2, 100, 8, 2048, "bf16", False),    # one thread sums 2 ranks, no residual
     (7, 16, 8, 7168, "fp32", True),      # odd R: one rank per group from 5 tokens on
     (8, 48, 8, 7168, "fp32", True),      # two groups of 4 ranks
-    (6, 50, 4, 4104, "bf16", True),      # two groups of 3 ranks, ragged row
+    (6, 50, 4, 7176, "bf16", True),      # two groups of 3 ranks, ragged row
 ]
 
 
@@ -286,12 +286,12 @@ def test_graph_capture_replay(cuda_lib, orc):
 @pytest.mark.parametrize("R,T,H,E,tile,P,plan", [
     # each thread sums the 8 ranks in sequence: one CTA per row, 2 passes
     (8, 1024, 4096, 512, 64, 16384, dict(lanes=1, splits=1, passes=2, cluster=1)),
-    # 4 groups of two ranks, 4 passes per thread, 8-CTA clusters
-    (8, 40, 16384, 64, 32, 1024, dict(lanes=4, splits=8, passes=4, cluster=8)),
     # 2 groups of four ranks, 2 passes per thread, 8-CTA clusters
-    (8, 48, 16384, 64, 32, 1024, dict(lanes=2, splits=8, passes=2, cluster=8)),
-    # one group per rank, 8 passes per thread, 8-CTA clusters
-    (4, 48, 32768, 64, 32, 1024, dict(lanes=4, splits=8, passes=8, cluster=8)),
+    (8, 40, 16384, 64, 32, 1024, dict(lanes=2, splits=8, passes=2, cluster=8)),
+    # 2 groups of two ranks, 4 passes per thread, 8-CTA clusters
+    (4, 48, 32768, 64, 32, 1024, dict(lanes=2, splits=8, passes=4, cluster=8)),
+    # one group per rank (odd R), 8 passes per thread, 8-CTA clusters
+    (5, 48, 16384, 64, 32, 1024, dict(lanes=5, splits=8, passes=8, cluster=8)),
 ])
 def test_large_sampled_rows(cuda_lib, orc, R, T, H, E, tile, P, plan):
     """Sizes with long rows or many tokens: sampled token rows against the
