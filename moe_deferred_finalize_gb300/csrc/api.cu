@@ -444,9 +444,14 @@ int pow2_bucket(int need) {
 // tokens alone fill the GPU, and each thread sums the ranks of its vector in
 // sequence (lanes = 1).  Slices start at kArSeqSlice vectors, one pass each;
 // with RMSNorm a row is one cluster of up to 16 CTAs of up to 256 threads,
-// the split halved while the grid exceeds 4 CTAs per SM (fewer, larger
-// clusters: R = 8, T = 256: 2 CTAs x 2 passes of 224 threads per row, 46.3
-// us against 47.9 us for 7 CTAs of 128 threads), up to 8 passes.  Measured
+// the split halved (up to 8 passes) until every CTA of the grid is resident
+// at once (CTAs per SM at 64 registers a thread for that CTA size).  Even a
+// small second wave costs more than the passes: R = 8, T = 160: 7 CTAs of
+// 128 threads per row, 29.6 us, against 37.2 us halved at 4 CTAs per SM;
+// T = 176 (just past one wave): 38.5 us for 2 CTAs x 2 passes of 224
+// threads against 43.0 us for 7 CTAs; T = 256: 46.3 against 47.9 us.
+// Splits stepped down one at a time (3 CTAs x 2 passes of 160 threads at
+// T = 176-288) measured 2-4 % slower than halving.  Measured
 // on GB300 at H = 7168 (one-shot / two-phase per rank, us): R = 8, T = 16:
 // rank pairs 8.9 / 6.5, one rank per group 9.2 / 8.5; T = 32: rank pairs
 // 11.1 / 7.7, one rank per group 15.3 / 8.8, sequential 17.2 / 8.0; T = 64:
@@ -475,11 +480,19 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
         } else {
             splits = ceil_div(nvec, kArSeqSlice);
             if (splits > kMaxCluster) splits = kMaxCluster;
-            while (splits > 1 && rows * splits > 4 * static_cast<int64_t>(num_sms)) {
+            // the most slices per row whose CTAs are all resident at once
+            // (64 registers a thread), halving the split otherwise
+            for (;;) {
+                if (splits <= 1) break;
+                const int sl = ceil_div(nvec, splits);
+                const int nv = round_up(ceil_div(sl, pow2_bucket(ceil_div(sl, kArSeqMaxThreads))), 32);
+                const int64_t resident = static_cast<int64_t>(num_sms) * (1024 / nv);
+                if (rows * splits <= resident) break;
                 const int half = ceil_div(splits, 2);
                 if (ceil_div(ceil_div(nvec, half), kArSeqMaxThreads) > kArMaxPasses) break;
                 splits = half;
             }
+
             slice = ceil_div(nvec, splits);
             passes = pow2_bucket(ceil_div(slice, kArSeqMaxThreads));
             if (passes > kArMaxPasses) {
