@@ -423,7 +423,7 @@ typedef struct {
 /*
  * moe_finalize_allreduce_plan -- the plan of the one-shot and phase-2 calls
  * (the two share it, which keeps their results bit-identical: lanes = R at
- * decode sizes, R / 2 from 5 tokens on when R > 4, 1 from 64 tokens on), or
+ * decode sizes, R / 2 or 2 from 8 tokens on when R > 4, 1 from 64 tokens on), or
  * of phase 1 with R = 1 and with_norm = 0.  Pure host computation.
  * Returns MOEF_ERR_SHAPE when an RMSNorm row is too long for one cluster
  * (more than 16 CTAs x 8 passes), else as moe_finalize_plan.

@@ -28,7 +28,7 @@
 // as one thread summing all ranks would.  Group 0 adds its own ranks'
 // partials in registers and the other groups' from shared memory, in rank
 // order, and finishes the vector.
-// Decode sizes use lanes = R (or R / 2 from 5 tokens on when R > 4, and 2
+// Decode sizes use lanes = R (or R / 2 from 8 tokens on when R > 4, and 2
 // from 44 tokens on when R >= 6); with many tokens, enough vectors to fill
 // the GPU, lanes = 1: each thread sums all ranks itself, with no exchange or
 // barrier per pass.  Phase 2 of a

@@ -276,7 +276,7 @@ def test_allreduce_argument_errors(mf):
 
 def test_allreduce_plans(mf):
     """Plan invariants over ranks, sizes and both epilogues: R groups of
-    threads per CTA at decode sizes (R / 2 groups of two ranks from 5 tokens
+    threads per CTA at decode sizes (R / 2 groups of two ranks from 8 tokens
     on when R > 4; one thread summing all ranks from 64 tokens on), every
     vector of a row covered, and with RMSNorm one cluster of at most 16 CTAs
     and at most 8 passes per thread."""
@@ -295,7 +295,7 @@ def test_allreduce_plans(mf):
                         # ranks in sequence once the tokens fill the GPU
                         seq = R > 1 and p["vec"] == 8 and T >= 64
                         groups = {R}                      # the layouts this size may take
-                        if p["vec"] == 8 and T > 4 and R % 2 == 0:
+                        if p["vec"] == 8 and T > 7 and R % 2 == 0:
                             if R > 4:
                                 groups.add(R // 2)
                             if R >= 4 and norm:

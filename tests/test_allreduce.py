@@ -107,6 +107,7 @@ CASES = [
     (3, 70, 4, 4104, "fp32", True),      # one thread sums 3 ranks, ragged row
     (2, 100, 8, 2048, "bf16", False),    # one thread sums 2 ranks, no residual
     (7, 16, 8, 7168, "fp32", True),      # odd R: one rank per group from 5 tokens on
+    (8, 7, 8, 7168, "fp32", True),       # decode plan up to 7 tokens: 16 CTAs of 512 threads a row
     (8, 48, 8, 7168, "fp32", True),      # two groups of 4 ranks
     (6, 50, 4, 7176, "bf16", True),      # two groups of 3 ranks, ragged row
 ]
