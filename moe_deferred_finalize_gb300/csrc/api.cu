@@ -452,7 +452,9 @@ int pow2_bucket(int need) {
 // sequence (lanes = 1).  Slices start at kArSeqSlice vectors, one pass each;
 // with RMSNorm a row is one cluster of up to 16 CTAs of up to 256 threads,
 // the split halved (up to 8 passes) until every CTA of the grid is resident
-// at once (CTAs per SM at 64 registers a thread for that CTA size).  Even a
+// at once (CTAs per SM at 64 registers a thread for that CTA size, whole
+// clusters per GPC: R = 8, T = 168 took 42.5 us on 7 CTAs a row, 1176 CTAs
+// that fit the SMs but not as 7-CTA clusters, against 38.0 us halved).  Even a
 // small second wave costs more than the passes: R = 8, T = 160: 7 CTAs of
 // 128 threads per row, 29.6 us, against 37.2 us halved at 4 CTAs per SM;
 // T = 176 (just past one wave): 38.5 us for 2 CTAs x 2 passes of 224
@@ -493,8 +495,14 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
                 if (splits <= 1) break;
                 const int sl = ceil_div(nvec, splits);
                 const int nv = round_up(ceil_div(sl, pow2_bucket(ceil_div(sl, kArSeqMaxThreads))), 32);
-                const int64_t resident = static_cast<int64_t>(num_sms) * (1024 / nv);
-                if (rows * splits <= resident) break;
+                // a row's CTAs are one cluster, placed within one of the GPU's
+                // 8 GPCs (num_sms / 8 SMs each): whole clusters per GPC, less
+                // one cluster's room for clusters of 4 CTAs or more (measured:
+                // 7-CTA clusters of 128 threads run in one wave at 160 rows but
+                // not at 168; 2-CTA clusters of 224 threads at 304 rows)
+                const int64_t per_gpc = static_cast<int64_t>(num_sms / 8) * (1024 / nv) -
+                                        (splits >= 4 ? splits : 0);
+                if (rows <= 8 * (per_gpc / splits)) break;
                 const int half = ceil_div(splits, 2);
                 if (ceil_div(ceil_div(nvec, half), kArSeqMaxThreads) > kArMaxPasses) break;
                 splits = half;
