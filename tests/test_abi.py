@@ -327,6 +327,16 @@ def test_allreduce_plans(mf):
     # not all be resident at once (T > ~35 for 256-thread CTAs, ~43 for 192)
     for R, T, lanes in ((8, 34, 4), (8, 35, 2), (4, 34, 4), (4, 35, 2), (6, 43, 3), (6, 44, 2)):
         assert mf.allreduce_plan(R, T, 7168, True)["lanes"] == lanes, (R, T)
+    # the decode plan (16 CTAs of 512 threads a row) up to T = 7
+    for R, T, lanes in ((8, 7, 8), (8, 8, 4), (6, 7, 6), (6, 8, 3)):
+        p = mf.allreduce_plan(R, T, 7168, True)
+        assert p["lanes"] == lanes and p["splits"] == (16 if T <= 7 else 14), (R, T, p)
+    # one thread summing all ranks: 7 CTAs a row while the rows' 7-CTA
+    # clusters are resident at once (160 rows), then 2 x 2 passes (up to 304
+    # rows of 2-CTA clusters), then 1 x 4 passes
+    for T, splits, passes in ((64, 7, 1), (160, 7, 1), (161, 2, 2), (304, 2, 2), (305, 1, 4)):
+        p = mf.allreduce_plan(8, T, 7168, True)
+        assert (p["lanes"], p["splits"], p["passes"]) == (1, splits, passes), (T, p)
     # many tokens: one thread per vector summing the 8 ranks, rows in 2
     # slices of 2 passes over 224 vectors
     p = mf.allreduce_plan(8, 256, 7168, True)
