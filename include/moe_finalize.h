@@ -423,8 +423,11 @@ typedef struct {
 /*
  * moe_finalize_allreduce_plan -- the plan of the one-shot and phase-2 calls
  * (the two share it, which keeps their results bit-identical: lanes = R at
- * decode sizes, R / 2 or 2 from 8 tokens on when R > 4, 1 from 64 tokens on), or
- * of phase 1 with R = 1 and with_norm = 0.  Pure host computation.
+ * decode sizes; for even R >= 4 from 8 tokens on, groups of ranks, R / 2 or
+ * 2 of them; 1 from 64 tokens on), or of phase 1 with R = 1 and
+ * with_norm = 0.  Pure host computation: the plan depends on its arguments
+ * only, num_sms included, so every call with the same arguments gets the
+ * same plan.
  * Returns MOEF_ERR_SHAPE when an RMSNorm row is too long for one cluster
  * (more than 16 CTAs x 8 passes), else as moe_finalize_plan.
  */
