@@ -581,8 +581,16 @@ template <int VEC, bool NORM, bool CLUSTER, int PASSES>
 cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms,
                         cudaStream_t stream) {
     const int cluster = CLUSTER ? plan.cluster : 1;
-    const bool small = plan.grid <= num_sms;
-    if (plan.lanes == p.ranks) {
+    // the 128-register builds (one CTA of 512 threads per SM) for grids of
+    // at most one CTA per SM whose clusters also fit: about 7 clusters of up
+    // to 16 such CTAs are resident at once
+    const int64_t rows = plan.grid / plan.splits;
+    const bool small = plan.grid <= num_sms && (plan.threads <= 256 || rows <= 7);
+    // phase 2 of a one-rank-per-group plan: in its rank groups, or with 4 or
+    // more ranks over a larger grid in the finishing threads alone, which
+    // load every rank's partial at once (R = 8, T = 8: 2.91 against 3.23
+    // us; R = 4, T = 24: 3.05 against 3.53 us)
+    if (plan.lanes == p.ranks && !(p.reduce && !small && p.ranks >= 4)) {
         // one rank per group: gathering, or phase 2 in rank groups
         static std::atomic<int> big[2][64];
         if (small)

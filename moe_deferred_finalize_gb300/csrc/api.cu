@@ -397,11 +397,17 @@ constexpr int kArSeqSlice = MOEF_AR_SEQ_SLICE;
 #define MOEF_AR_SEQ_MAX_THREADS 256
 #endif
 // Tokens up to which a row takes the decode plan (CTAs of up to 512 threads,
-// one cluster of up to 16 CTAs a row, one CTA per SM): about 7 such clusters
-// are resident at once (launch__cluster_max_active).  R = 8: T = 5 / 7 take
-// 4.80 / 5.20 us against 7.17 / 7.35 us with the rank pairs of larger T;
-// R = 6, T = 5: 4.53 against 7.02 us; R = 2 and 4: 0.05-0.17 us faster.
-constexpr int kArDecodeTokens = 7;
+// one cluster of up to 16 CTAs a row, one CTA per SM in the 128-register
+// build): about 7 such clusters are resident at once
+// (launch__cluster_max_active).  R = 8: T = 5 / 7 take 4.80 / 5.20 us
+// against 7.17 / 7.35 us with the rank pairs of larger T; R = 6, T = 5: 4.53
+// against 7.02 us; R = 2 and 4: 0.05-0.17 us faster.
+// With more than kArMidLanes ranks, where the alternative is rank pairs, up
+// to 14 tokens: past 7 the kernels take their 64-register build, two CTAs
+// per SM, and twice the clusters fit (R = 8, T = 8 / 14: 6.12 / 6.83 us
+// against 7.53 / 8.18 us with rank pairs, the two-phase form unchanged).
+constexpr int kArDecodeTokensBase = 7;
+constexpr int kArDecodeTokensWide = 14;
 constexpr int kArMidLanes = MOEF_AR_MID_LANES;
 constexpr int kArSeqMaxThreads = MOEF_AR_SEQ_MAX_THREADS;
 
@@ -473,6 +479,7 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
     const int vec = (vec_ok && H % 8 == 0) ? 8 : 1;
     const int nvec = H / vec;
     const int64_t rows = T > 0 ? T : 1;
+    const int kArDecodeTokens = R > kArMidLanes ? kArDecodeTokensWide : kArDecodeTokensBase;
     int lanes = R, nvc = 0, splits = 0, slice = 0, passes = 0;
     if (R > 1 && vec == 8 && T >= kArSeqMinTokens) {
         lanes = 1;

@@ -327,10 +327,12 @@ def test_allreduce_plans(mf):
     # not all be resident at once (T > ~35 for 256-thread CTAs, ~43 for 192)
     for R, T, lanes in ((8, 34, 4), (8, 35, 2), (4, 34, 4), (4, 35, 2), (6, 43, 3), (6, 44, 2)):
         assert mf.allreduce_plan(R, T, 7168, True)["lanes"] == lanes, (R, T)
-    # the decode plan (16 CTAs of 512 threads a row) up to T = 7
-    for R, T, lanes in ((8, 7, 8), (8, 8, 4), (6, 7, 6), (6, 8, 3)):
+    # the decode plan (16 CTAs a row, one rank per thread group) up to T = 7,
+    # or up to 14 with more than 4 ranks (whose alternative is rank pairs)
+    for R, T, lanes in ((4, 7, 4), (4, 8, 4), (8, 14, 8), (8, 15, 4), (6, 14, 6), (6, 15, 3)):
         p = mf.allreduce_plan(R, T, 7168, True)
-        assert p["lanes"] == lanes and p["splits"] == (16 if T <= 7 else 14), (R, T, p)
+        decode = T <= (14 if R > 4 else 7)
+        assert p["lanes"] == lanes and p["splits"] == (16 if decode else 14), (R, T, p)
     # one thread summing all ranks: 7 CTAs a row while the rows' 7-CTA
     # clusters are resident at once (160 rows), then 2 x 2 passes (up to 304
     # rows of 2-CTA clusters), then 1 x 4 passes

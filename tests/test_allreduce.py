@@ -101,13 +101,14 @@ CASES = [
     (3, 5, 2, 64, "fp32", True),         # a row shorter than a warp per rank: padded to whole warps
     (5, 2, 3, 40, "bf16", True),         # scalar path, 5 ranks, 40 values a row
     (6, 16, 8, 7168, "fp32", True),      # 3 groups of rank pairs
-    (6, 12, 8, 7168, "bf16", False),     # rank pairs, no residual
+    (6, 20, 8, 7168, "bf16", False),     # rank pairs, no residual
     (8, 20, 4, 4104, "fp32", True),      # rank pairs over a ragged row
     (6, 64, 8, 7168, "packed", True),    # one thread sums 6 ranks
     (3, 70, 4, 4104, "fp32", True),      # one thread sums 3 ranks, ragged row
     (2, 100, 8, 2048, "bf16", False),    # one thread sums 2 ranks, no residual
     (7, 16, 8, 7168, "fp32", True),      # odd R: one rank per group from 5 tokens on
-    (8, 7, 8, 7168, "fp32", True),       # decode plan up to 7 tokens: 16 CTAs of 512 threads a row
+    (8, 7, 8, 7168, "fp32", True),       # decode plan: 16 CTAs of 512 threads a row
+    (8, 12, 8, 7168, "fp32", True),      # decode plan past 7 tokens (64-register build)
     (8, 48, 8, 7168, "fp32", True),      # two groups of 4 ranks
     (6, 50, 4, 7176, "bf16", True),      # two groups of 3 ranks, ragged row
 ]
