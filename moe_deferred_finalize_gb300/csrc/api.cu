@@ -386,7 +386,7 @@ constexpr int kArMaxPasses = 8;
 #ifndef MOEF_AR_SEQ_SLICE
 #define MOEF_AR_SEQ_SLICE 128
 #endif
-// Largest rank group count past kArDecodeTokens (R > this: groups of 2 ranks).
+// Largest rank group count past the decode sizes (R > this: groups of 2 ranks).
 #ifndef MOEF_AR_MID_LANES
 #define MOEF_AR_MID_LANES 4
 #endif
@@ -422,25 +422,26 @@ int pow2_bucket(int need) {
 // Plan of the all-reduce-fused kernels.  At decode sizes a CTA holds R
 // groups of threads, one per rank, each thread obtaining one rank's partial
 // of one vector per pass, so that every rank's row loads are in flight at
-// once (lanes = R); past kArDecodeTokens, with more than kArMidLanes ranks
+// once (lanes = R); past the decode sizes, with more than kArMidLanes ranks
 // and 16-byte vectors, R / 2 groups of two ranks each:
 //  * without RMSNorm, 128 threads per CTA (`lanes` groups of 128 / lanes, at
 //    least 16 threads), one vector per thread: slices of 128 / lanes vectors;
 //  * with RMSNorm, one CTA or one cluster of up to 16 CTAs finishes a row.
 //    Each extra pass over a slice costs a full chain of loads, barrier and
-//    epilogue (about 2.8 us at R = 8, T = 1), so a few tokens (up to
-//    kArDecodeTokens) take CTAs of
-//    up to 512 threads (`lanes` groups of 512 / lanes, at most 256), enough for one
-//    pass, and with R > 1 a split row over a full cluster of 16 (slices of
-//    at least 32 vectors), so that more SMs share the ranks' rows: with R =
-//    8 at H = 7168, 16 CTAs of 8 x 64 threads (T = 1: 4.28 -> 4.24 us
-//    against 14 CTAs; R = 2: 4.19 -> 3.91 us against 4 CTAs of 2 x 224
-//    threads; R = 4: 4.31 -> 4.04 us; H = 4096: 0.05-0.24 us faster).  From T = 8 on
-//    CTAs of 256 threads win even with a second pass (R = 4, T = 16: 14 x
-//    256 threads 5.6 us vs 7 x 512 threads 9.3 us; R = 8: 16 x 224 threads
-//    9.2 us vs 14 x 512 threads 11.9 us).  The split is halved while the grid
-//    exceeds 4 CTAs per SM, each thread then taking up to 8 passes.
-// Past kArDecodeTokens up to the sequential-ranks plans, R >= 4 ranks (even) go in
+//    epilogue (about 2.8 us at R = 8, T = 1), so the decode sizes (up to
+//    kArDecodeTokensBase tokens, kArDecodeTokensWide with R > kArMidLanes)
+//    take CTAs of up to 512 threads (`lanes` groups of 512 / lanes, at most
+//    256), enough for one pass, and with R > 1 a split row over a full
+//    cluster of 16 (slices of at least 32 vectors), so that more SMs share
+//    the ranks' rows: with R = 8 at H = 7168, 16 CTAs of 8 x 64 threads
+//    (T = 1: 4.28 -> 4.24 us against 14 CTAs; R = 2: 4.19 -> 3.91 us against
+//    4 CTAs of 2 x 224 threads; R = 4: 4.31 -> 4.04 us; H = 4096: 0.05-0.24
+//    us faster).  Past the decode sizes CTAs of 256 threads win even with a
+//    second pass (R = 4, T = 16: 14 x 256 threads 5.6 us vs 7 x 512 threads
+//    9.3 us; R = 8: 16 x 224 threads 9.2 us vs 14 x 512 threads 11.9 us).
+//    The split is halved while the grid exceeds 4 CTAs per SM, each thread
+//    then taking up to 8 passes.
+// Past the decode sizes up to the sequential-ranks plans, R >= 4 ranks (even) go in
 // two groups of R / 2 (CTAs of 2 x 128 threads) once the plan above would
 // not have all its rows' clusters resident at once, or would need a second
 // pass.  14-CTA clusters of 256-thread CTAs fit about 35 at a time: R = 8,
@@ -479,7 +480,7 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
     const int vec = (vec_ok && H % 8 == 0) ? 8 : 1;
     const int nvec = H / vec;
     const int64_t rows = T > 0 ? T : 1;
-    const int kArDecodeTokens = R > kArMidLanes ? kArDecodeTokensWide : kArDecodeTokensBase;
+    const int decode_tokens = R > kArMidLanes ? kArDecodeTokensWide : kArDecodeTokensBase;
     int lanes = R, nvc = 0, splits = 0, slice = 0, passes = 0;
     if (R > 1 && vec == 8 && T >= kArSeqMinTokens) {
         lanes = 1;
@@ -548,7 +549,7 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
             }
             pa = ceil_div(sl, nv);
         } else {
-            int nvc_max = (T <= kArDecodeTokens ? kArMaxThreads : kArMaxThreads / 2) / ln;
+            int nvc_max = (T <= decode_tokens ? kArMaxThreads : kArMaxThreads / 2) / ln;
             if (nvc_max > 256) nvc_max = 256;
             nvc_max = nvc_max / 32 * 32;
             sp = ceil_div(nvec, nvc_max);
@@ -557,7 +558,7 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
             // more SMs share the ranks' rows.  A row that fits one CTA stays
             // there: a cluster's barrier costs more than it gains (R = 2,
             // H = 2048: 3.23 us in one CTA, 3.63 us over 8)
-            if (T <= kArDecodeTokens && R > 1 && sp > 1 && sp < kMaxCluster) {
+            if (T <= decode_tokens && R > 1 && sp > 1 && sp < kMaxCluster) {
                 const int wide = nvec / 32 < kMaxCluster ? nvec / 32 : kMaxCluster;
                 if (wide > sp) sp = wide;
             }
@@ -581,14 +582,14 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
         return MOEF_OK;
     };
     if (lanes > 1 || R == 1) {
-        if (T > kArDecodeTokens && R > kArMidLanes && R % 2 == 0 && vec == 8) lanes = R / 2;
+        if (T > decode_tokens && R > kArMidLanes && R % 2 == 0 && vec == 8) lanes = R / 2;
         moef_status st = group_plan(lanes, &nvc, &splits, &slice, &passes);
         if (st != MOEF_OK) return st;
         // Two groups of R / 2 ranks instead, when the rows' clusters would
         // not all be resident at once (CTAs of 64 registers a thread, about
         // 4/5 of the SMs' room usable by clusters, as measured with
         // launch__cluster_max_active) or would need a second pass
-        if (with_norm && R >= 4 && R % 2 == 0 && vec == 8 && T > kArDecodeTokens && lanes > 2 &&
+        if (with_norm && R >= 4 && R % 2 == 0 && vec == 8 && T > decode_tokens && lanes > 2 &&
             splits > 1) {
             const int64_t per_sm = 1024 / (static_cast<int64_t>(lanes) * nvc);
             const int64_t fit = static_cast<int64_t>(num_sms) * per_sm * 4 / 5 / splits;
@@ -614,7 +615,8 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
     if (grid > 0x7FFFFFFFLL) return MOEF_ERR_SHAPE;
     const int vbytes = vec == 8 ? 16 : 2;
     // the exchanged partials of a pass: every group's with one rank per group,
-    // ranks 2 .. R-1 with pairs, none when one thread sums all ranks
+    // ranks c .. R-1 with groups of c = R / lanes ranks, none when one thread
+    // sums all ranks
     const int exchanged = lanes == R ? (lanes > 1 ? R : 0) : lanes > 1 ? R - R / lanes : 0;
     int64_t smem = static_cast<int64_t>(sizeof(float)) * vec * exchanged * nvc +
                    (with_norm ? static_cast<int64_t>(passes) * nvc * vbytes : 0);
