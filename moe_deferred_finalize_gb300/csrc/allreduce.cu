@@ -177,7 +177,8 @@ __device__ __forceinline__ void norm_tail(const ArParams &p, bool finisher, int 
 #pragma unroll
     for (int qq = 0; qq < PASSES; ++qq) {
         const int v = v_begin + qq * nvc + j;
-        if (finisher && v < v_end) g[qq] = Ops::load_reused(p.gamma + static_cast<int64_t>(v) * VEC);
+        if (finisher && v < v_end)
+            g[qq] = Ops::load_reused(p.gamma + static_cast<int64_t>(v) * VEC);
     }
     ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
@@ -619,9 +620,9 @@ cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms
                                     big[1], p, plan.grid, plan.threads, plan.smem_bytes, cluster,
                                     stream);
         if (p.ranks % plan.lanes == 0)
-            return launch_ar_kernel(finalize_ar_multi_kernel<VEC, NORM, CLUSTER, PASSES, kRankGroups>,
-                                    big[0], p, plan.grid, plan.threads, plan.smem_bytes, cluster,
-                                    stream);
+            return launch_ar_kernel(
+                finalize_ar_multi_kernel<VEC, NORM, CLUSTER, PASSES, kRankGroups>, big[0], p,
+                plan.grid, plan.threads, plan.smem_bytes, cluster, stream);
     }
     return cudaErrorInvalidValue;
 }

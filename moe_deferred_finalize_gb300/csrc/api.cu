@@ -502,7 +502,8 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
             for (;;) {
                 if (splits <= 1) break;
                 const int sl = ceil_div(nvec, splits);
-                const int nv = round_up(ceil_div(sl, pow2_bucket(ceil_div(sl, kArSeqMaxThreads))), 32);
+                const int pa = pow2_bucket(ceil_div(sl, kArSeqMaxThreads));
+                const int nv = round_up(ceil_div(sl, pa), 32);
                 // a row's CTAs are one cluster, placed within one of the GPU's
                 // 8 GPCs (num_sms / 8 SMs each): whole clusters per GPC, less
                 // one cluster's room for clusters of 4 CTAs or more (measured:
