@@ -355,7 +355,9 @@ finalize_ar_kernel(const __grid_constant__ ArParams p) {
 // rank order itself, no exchange).
 enum { kRankGroups = 1, kAllRanks = 2 };
 
-template <int VEC, bool NORM, bool CLUSTER, int PASSES, int MODE>
+// KC: K when fixed at compile time (top-8: no predicated slots, and the
+// rank-group build then fits 64 registers without spilling), else 0.
+template <int VEC, bool NORM, bool CLUSTER, int PASSES, int MODE, int KC>
 __global__ void __launch_bounds__(kArMaxThreads, 2)
 finalize_ar_multi_kernel(const __grid_constant__ ArParams p) {
     using Ops = VecOps<VEC>;
@@ -385,7 +387,7 @@ finalize_ar_multi_kernel(const __grid_constant__ ArParams p) {
     const int S = p.splits;
     const int t = blockIdx.x / S;
     const int split = blockIdx.x - t * S;
-    const int K = p.K;
+    const int K = KC ? KC : p.K;
     const int64_t tok = static_cast<int64_t>(t) * p.H;
     const int v_begin = split * p.slice;
     const int v_end = min(v_begin + p.slice, p.nvec);
@@ -578,6 +580,20 @@ cudaError_t launch_ar_kernel(Kern kern, std::atomic<int> (&big)[64], const ArPar
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// The multi-rank kernel (16-byte vectors): one thread summing all ranks
+// (lanes = 1) or groups of several ranks.
+template <bool NORM, bool CLUSTER, int PASSES, int KC>
+cudaError_t launch_multi(const ArParams &p, const moef_ar_plan &plan, int cluster,
+                         cudaStream_t stream) {
+    static std::atomic<int> big[2][64];
+    if (plan.lanes == 1)
+        return launch_ar_kernel(finalize_ar_multi_kernel<8, NORM, CLUSTER, PASSES, kAllRanks, KC>,
+                                big[1], p, plan.grid, plan.threads, plan.smem_bytes, cluster,
+                                stream);
+    return launch_ar_kernel(finalize_ar_multi_kernel<8, NORM, CLUSTER, PASSES, kRankGroups, KC>,
+                            big[0], p, plan.grid, plan.threads, plan.smem_bytes, cluster, stream);
+}
+
 template <int VEC, bool NORM, bool CLUSTER, int PASSES>
 cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms,
                         cudaStream_t stream) {
@@ -614,15 +630,11 @@ cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms
     }
     // groups of several ranks: planned for 16-byte vectors only
     if constexpr (VEC == 8) {
-        static std::atomic<int> big[2][64];
-        if (plan.lanes == 1)
-            return launch_ar_kernel(finalize_ar_multi_kernel<VEC, NORM, CLUSTER, PASSES, kAllRanks>,
-                                    big[1], p, plan.grid, plan.threads, plan.smem_bytes, cluster,
-                                    stream);
-        if (p.ranks % plan.lanes == 0)
-            return launch_ar_kernel(
-                finalize_ar_multi_kernel<VEC, NORM, CLUSTER, PASSES, kRankGroups>, big[0], p,
-                plan.grid, plan.threads, plan.smem_bytes, cluster, stream);
+        if (plan.lanes == 1 || p.ranks % plan.lanes == 0) {
+            if (p.K == 8)
+                return launch_multi<NORM, CLUSTER, PASSES, 8>(p, plan, cluster, stream);
+            return launch_multi<NORM, CLUSTER, PASSES, 0>(p, plan, cluster, stream);
+        }
     }
     return cudaErrorInvalidValue;
 }
