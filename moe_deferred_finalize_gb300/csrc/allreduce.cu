@@ -231,7 +231,8 @@ __device__ __forceinline__ void norm_tail(const ArParams &p, bool finisher, int 
 // (Measured on GB300: building the phase-1/one-shot-only form of this
 // kernel, without the phase-2 branch, made the decode calls 0.1-0.35 us
 // slower.)
-template <int VEC, bool NORM, bool CLUSTER, int PASSES, int MINB>
+// KC: K when fixed at compile time (top-8), else 0.
+template <int VEC, bool NORM, bool CLUSTER, int PASSES, int MINB, int KC>
 __global__ void __launch_bounds__(kArMaxThreads, MINB)
 finalize_ar_kernel(const __grid_constant__ ArParams p) {
     using Ops = VecOps<VEC>;
@@ -257,7 +258,7 @@ finalize_ar_kernel(const __grid_constant__ ArParams p) {
     const int S = p.splits;
     const int t = blockIdx.x / S;
     const int split = blockIdx.x - t * S;
-    const int K = p.K;
+    const int K = KC ? KC : p.K;
     const int64_t tok = static_cast<int64_t>(t) * p.H;
     const int v_begin = split * p.slice;
     const int v_end = min(v_begin + p.slice, p.nvec);
@@ -608,12 +609,18 @@ cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms
     // load every rank's partial at once (R = 8, T = 8: 2.91 against 3.23
     // us; R = 4, T = 24: 3.05 against 3.53 us)
     if (plan.lanes == p.ranks && !(p.reduce && !small && p.ranks >= 4)) {
-        // one rank per group: gathering, or phase 2 in rank groups
-        static std::atomic<int> big[2][64];
+        // one rank per group: gathering, or phase 2 in rank groups.  Top-8
+        // gathers over large grids take the build with K fixed (R = 8, T = 8:
+        // 6.09 -> 5.74 us; R = 4, T = 32: 7.03 -> 6.41 us); the small-grid
+        // build, a chain of latencies, measured 0.2 us slower with it.
+        static std::atomic<int> big[3][64];
         if (small)
-            return launch_ar_kernel(finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES, 1>, big[1], p,
-                                    plan.grid, plan.threads, plan.smem_bytes, cluster, stream);
-        return launch_ar_kernel(finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES, 2>, big[0], p,
+            return launch_ar_kernel(finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES, 1, 0>, big[1],
+                                    p, plan.grid, plan.threads, plan.smem_bytes, cluster, stream);
+        if (VEC == 8 && p.K == 8 && !p.reduce)
+            return launch_ar_kernel(finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES, 2, 8>, big[2],
+                                    p, plan.grid, plan.threads, plan.smem_bytes, cluster, stream);
+        return launch_ar_kernel(finalize_ar_kernel<VEC, NORM, CLUSTER, PASSES, 2, 0>, big[0], p,
                                 plan.grid, plan.threads, plan.smem_bytes, cluster, stream);
     }
     if (p.reduce) {
