@@ -537,9 +537,9 @@ def allreduce_bytes(R, T, K, H, wbytes=4):
 
 def allreduce_latency(mf, device, R, T, peak, calls=1000):
     """µs per call of the all-reduce-fused finalize at decode size T over R
-    ranks' buffer sets on this one GPU (CUDA-graph replay, every call on
-    buffer copies no other call in the pass touched, the copies together
-    larger than L2):
+    ranks' buffer sets on this one GPU (CUDA-graph replay; every call on
+    buffer copies no other call in the pass touched, the copies a timed
+    call rotates over together at least twice the L2):
 
       * one-shot: one launch reading every rank's rows (what each rank
         would run, with the peers' rows read over NVLink instead of HBM);
@@ -547,74 +547,100 @@ def allreduce_latency(mf, device, R, T, peak, calls=1000):
         all R partials (the other R - 1 already in place);
       * phase 1 and phase 2 alone;
       * the plain finalize of one rank's operands with residual + RMSNorm,
-        for comparison with R of them."""
+        for comparison with R of them.
+
+    The one-shot rotates over copies of every rank's operands; the other
+    calls touch far fewer bytes and rotate over copies of their own (rank
+    0's operands, the R partials, residual and outputs), as many as the
+    smallest of their working sets needs."""
     g = W.tp_decode(R, T)
     K, H = g.K, g.H
     nbytes = allreduce_bytes(R, T, K, H)
-    C = int(min(max(2, np.ceil(2 * L2_BYTES / nbytes)), 512))
+    p1_bytes = T * K * H * 2 + T * H * 2 + T * K * 8 + T * H * 4
+    p2_bytes = R * T * H * 4 + 3 * T * H * 2 + H * 2
 
-    def rep(a):   # C copies at distinct addresses
+    def n_copies(b):
+        return int(min(max(2, np.ceil(2 * L2_BYTES / b)), 4096))
+
+    C, Cr = n_copies(nbytes), n_copies(min(p1_bytes, p2_bytes))
+
+    def rep(a, n):   # n copies at distinct addresses
         t = host_tensor(np.ascontiguousarray(a)).to(device)
-        return t.unsqueeze(0).expand(C, *t.shape).contiguous()
+        return t.unsqueeze(0).expand(n, *t.shape).contiguous()
 
-    ranks = [{"permuted_out": rep(wl.permuted_out), "idx_map": rep(wl.idx),
-              "weights": rep(wl.weights), "shared_out": rep(wl.shared)} for wl in g.ranks]
-    res_in, gamma = rep(g.residual), host_tensor(g.gamma).to(device)
-    r_out = torch.empty((C, T, H), dtype=torch.bfloat16, device=device)
-    n_out = torch.empty_like(r_out)
-    partials = torch.empty((C, R, T, H), dtype=torch.float32, device=device)
-    sets = [([{k: v[c] for k, v in rk.items()} for rk in ranks],
-             dict(residual=res_in[c], gamma=gamma, eps=g.eps, residual_out=r_out[c],
-                  norm_out=n_out[c], write_out=False), partials[c]) for c in range(C)]
+    keys = ("permuted_out", "idx_map", "weights", "shared_out")
+
+    def operands(wl, n):
+        return dict(zip(keys, (rep(a, n) for a in (wl.permuted_out, wl.idx, wl.weights,
+                                                      wl.shared))))
+
+    def epilogue_sets(n):
+        res_in, r_out = rep(g.residual, n), torch.empty((n, T, H), dtype=torch.bfloat16,
+                                                         device=device)
+        n_out = torch.empty_like(r_out)
+        return [dict(residual=res_in[c], gamma=gamma, eps=g.eps, residual_out=r_out[c],
+                     norm_out=n_out[c], write_out=False) for c in range(n)]
+
+    gamma = host_tensor(g.gamma).to(device)
+    ranks = [operands(wl, C) for wl in g.ranks]
+    one_sets = list(zip([[{k: v[c] for k, v in rk.items()} for rk in ranks] for c in range(C)],
+                        epilogue_sets(C)))
+    own = operands(g.ranks[0], Cr)
+    partials = torch.empty((Cr, R, T, H), dtype=torch.float32, device=device)
+    rank_sets = list(zip([{k: v[c] for k, v in own.items()} for c in range(Cr)],
+                         epilogue_sets(Cr), partials))
     scale = g.routed_scale
 
     def oneshot():
-        for rks, ep, _ in sets:
+        for rks, ep in one_sets:
             mf.moe_finalize_allreduce(rks, g.wkind, routed_scale=scale, **ep)
 
-    def phase1(rks, part):
-        r0 = rks[0]
+    def phase1(r0, part):
         mf.moe_finalize_partial(r0["permuted_out"], r0["idx_map"], r0["weights"], g.wkind,
                                 r0["shared_out"], routed_scale=scale, partial=part[0])
 
     def two_phase_rank():
-        for rks, ep, part in sets:
-            phase1(rks, part)
+        for r0, ep, part in rank_sets:
+            phase1(r0, part)
             mf.moe_finalize_allreduce_reduce(list(part), **ep)
 
     def phase1_only():
-        for rks, _, part in sets:
-            phase1(rks, part)
+        for r0, _, part in rank_sets:
+            phase1(r0, part)
 
     def phase2_only():
-        for _, ep, part in sets:
+        for _, ep, part in rank_sets:
             mf.moe_finalize_allreduce_reduce(list(part), **ep)
 
     def standalone():
-        for rks, ep, _ in sets:
-            r0 = rks[0]
+        for r0, ep, _ in rank_sets:
             mf.moe_finalize(r0["permuted_out"], r0["idx_map"], r0["weights"], g.wkind,
                             r0["shared_out"], routed_scale=scale, **ep)
 
-    for rks, _, part in sets:                 # every partial in place once
-        for r, rk in enumerate(rks):
-            mf.moe_finalize_partial(rk["permuted_out"], rk["idx_map"], rk["weights"], g.wkind,
-                                    rk["shared_out"], routed_scale=scale, partial=part[r])
+    # every partial in place once: rank r's from its operands (copy 0 of the
+    # one-shot's), the same values in every copy
+    for r in range(R):
+        rk = {k: v[0] for k, v in ranks[r].items()}
+        mf.moe_finalize_partial(rk["permuted_out"], rk["idx_map"], rk["weights"], g.wkind,
+                                rk["shared_out"], routed_scale=scale, partial=partials[0, r])
+    partials[1:].copy_(partials[0].unsqueeze(0).expand(Cr - 1, R, T, H))
     oneshot()
     torch.cuda.synchronize(device)
-    n_pass = max(1, calls // C)
-    t = {name: graph_us(fn, device, C, n_pass)
-         for name, fn in (("one_shot", oneshot), ("two_phase_rank", two_phase_rank),
-                          ("phase1", phase1_only), ("phase2", phase2_only),
-                          ("standalone_finalize", standalone))}
+    t = {name: graph_us(fn, device, n, max(1, calls // n))
+         for name, fn, n in (("one_shot", oneshot, C), ("two_phase_rank", two_phase_rank, Cr),
+                             ("phase1", phase1_only, Cr), ("phase2", phase2_only, Cr),
+                             ("standalone_finalize", standalone, Cr))}
     out = {f"us_{k}": round(v, 3) for k, v in t.items()}
     out.update({"R": R, "T": T, "K": K, "H": H, "bytes_one_shot": nbytes,
                 "GBps_one_shot": round(nbytes / (t["one_shot"] * 1e-6) / 1e9, 1),
                 "frac_one_shot": round(nbytes / (t["one_shot"] * 1e-6) / 1e9 / peak, 4),
+                "bytes_phase2": p2_bytes,
+                "frac_phase2": round(p2_bytes / (t["phase2"] * 1e-6) / 1e9 / peak, 4),
                 "us_R_x_standalone_finalize": round(R * t["standalone_finalize"], 3),
-                "copies": C, "calls": n_pass * C,
+                "copies": C, "copies_one_rank": Cr,
+                "calls": max(1, calls // C) * C,
                 "plan": mf.allreduce_plan(R, T, H, True)})
-    del ranks, res_in, r_out, n_out, partials, sets
+    del ranks, one_sets, own, partials, rank_sets
     torch.cuda.empty_cache()
     return out
 

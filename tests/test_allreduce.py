@@ -150,6 +150,30 @@ def test_phase1_partial_within_its_fp32_bound(cuda_lib, orc):
         assert (err <= bound).all(), float((err / bound).max())
 
 
+def test_partials_at_16_byte_aligned_addresses(cuda_lib):
+    """Partials at addresses that are 16-byte but not 32-byte aligned (the
+    16-byte path's minimum): phase 1 writes the same bits there, and phase 2
+    reading them gives the same outputs."""
+    g = W.tp_decode(2, 16)
+    rd = ranks_dev(g)
+    T, H = g.T, g.H
+    ref, aligned = two_phase(cuda_lib, g, rd)
+    shifted = []
+    for r in rd:
+        buf = torch.empty(T * H + 4, dtype=torch.float32, device="cuda")
+        part = buf[4:].view(T, H)
+        assert part.data_ptr() % 32 == 16
+        cuda_lib.moe_finalize_partial(r["permuted_out"], r["idx_map"], r["weights"], g.wkind,
+                                      r["shared_out"], routed_scale=g.routed_scale,
+                                      partial=part)
+        shifted.append(part)
+    res = cuda_lib.moe_finalize_allreduce_reduce(shifted, **epilogue_dev(g))
+    torch.cuda.synchronize()
+    for a, b in zip(aligned, shifted):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert_same_bits(res, ref, "16-byte-aligned partials")
+
+
 def test_one_rank_is_the_plain_finalize(cuda_lib, orc):
     """R = 1: out and residual_out equal moe_finalize's bit for bit (same fp32
     operations in the same order); norm_out within tolerance of the oracle."""
