@@ -207,6 +207,30 @@ def test_plan_invariants(mf):
                         assert p["cluster"] == 1
 
 
+def test_plans_every_token_count(mf):
+    """The plain finalize's plan at every token count from 1 to 640 and at
+    the powers of two up to 2^16 (the decode split, the cluster and
+    threads-per-CTA switches), for top-1/2/6/8/9 routing at common hidden
+    sizes: every plan is one the launcher accepts."""
+    Ts = list(range(1, 641)) + [2 ** i for i in range(10, 17)]
+    for H in (2048, 4096, 5120, 7168, 8192):
+        for K in (1, 2, 6, 8, 9):
+            for norm in (False, True):
+                for T in Ts:
+                    p = mf.plan(T, K, H, norm)
+                    where = (T, K, H, norm, p)
+                    nvec = H // p["vec"]
+                    assert p["vec"] == 8, where
+                    assert p["splits"] * p["slice"] >= nvec > (p["splits"] - 1) * p["slice"], where
+                    assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 256, where
+                    assert p["vpt"] in (1, 2, 4, 8) and p["grid"] == T * p["splits"], where
+                    if norm:
+                        assert p["threads"] * p["vpt"] >= p["slice"], where
+                        assert p["cluster"] == p["splits"] <= 16, where
+                    else:
+                        assert p["cluster"] == 1, where
+
+
 def test_allreduce_argument_errors(mf):
     """The all-reduce-fused entry points check every rank's operands and the
     epilogue before any CUDA call."""
@@ -348,6 +372,38 @@ def test_allreduce_plans(mf):
         mf.allreduce_plan(8, 1, 8 * 8 * 16 * 64 + 8, True)    # longer than 16 CTAs x 8 passes
     with pytest.raises(mf.MoefError):
         mf.allreduce_plan(9, 1, 7168, True)
+
+
+def test_allreduce_plans_every_token_count(mf):
+    """Every token count from 1 to 640 (all the plan's switch points: the
+    decode limits, the two-group and all-ranks layouts, the cluster and
+    pass changes) at the hidden sizes of common models: each plan is one the
+    launcher accepts and the kernels were built for (lanes dividing R, whole
+    warps with RMSNorm, 1/2/4/8 passes covering the slice, at most 16 CTAs
+    a cluster, groups of several ranks only with 16-byte vectors), and the
+    size a plan picks never needs more shared memory than a CTA gets
+    without opting in."""
+    for R in range(1, 9):
+        for H in (2048, 4096, 5120, 6144, 7168, 8192):
+            for norm in (False, True):
+                for T in range(1, 641):
+                    p = mf.allreduce_plan(R, T, H, norm)
+                    lanes, nvc, vec = p["lanes"], p["nvc"], p["vec"]
+                    where = (R, T, H, norm, p)
+                    assert R % lanes == 0 and (lanes in (1, R) or vec == 8), where
+                    assert p["threads"] == lanes * nvc <= 512, where
+                    assert p["splits"] * p["slice"] >= H // vec, where
+                    assert p["grid"] == T * p["splits"], where
+                    assert p["smem_bytes"] <= 48 * 1024, where
+                    if norm:
+                        assert p["threads"] % 32 == 0, where
+                        assert p["passes"] in (1, 2, 4, 8), where
+                        assert p["passes"] * nvc >= p["slice"], where
+                        assert p["cluster"] == p["splits"] <= 16, where
+                        # phase 2's kept vectors fit its shared memory too
+                        assert p["passes"] * nvc * 16 <= 48 * 1024, where
+                    else:
+                        assert p["cluster"] == 1, where
 
 
 def test_allreduce_parity_shapes_cover_every_layout(mf):

@@ -111,6 +111,20 @@ CASES = [
     (8, 12, 8, 7168, "fp32", True),      # decode plan past 7 tokens (64-register build)
     (8, 48, 8, 7168, "fp32", True),      # two groups of 4 ranks
     (6, 50, 4, 7176, "bf16", True),      # two groups of 3 ranks, ragged row
+    # both sides of every switch of the plan at H = 7168 (the plan does not
+    # depend on K; K = 2 keeps the large-T operands small)
+    (8, 14, 8, 7168, "fp32", True),      # last decode-plan size
+    (8, 15, 8, 7168, "packed", True),    # first rank-pair size
+    (8, 34, 8, 7168, "fp32", True),      # last rank-pair size
+    (8, 35, 8, 7168, "bf16", True),      # first two-group size
+    (6, 43, 8, 7168, "fp32", True),      # R = 6: last rank-pair size
+    (6, 44, 8, 7168, "fp32", True),      # R = 6: first two-group size
+    (8, 63, 8, 7168, "fp32", True),      # last two-group size
+    (8, 64, 8, 7168, "fp32", True),      # first all-ranks size
+    (8, 160, 2, 7168, "fp32", True),     # 7 CTAs a row, one wave
+    (8, 161, 2, 7168, "bf16", True),     # 2 CTAs a row, 2 passes
+    (8, 304, 2, 7168, "fp32", True),     # last 2-CTA size
+    (8, 305, 2, 7168, "packed", True),   # a row per CTA, 4 passes
 ]
 
 
