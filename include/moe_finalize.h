@@ -375,7 +375,10 @@ moef_status moe_finalize_allreduce(const moef_rank_inputs *ranks, int R,
  * (see above), written unrounded as fp32 [T, H] into `partial` (4-byte
  * aligned; 16-byte aligned with H % 8 == 0 for the vector path; not
  * overlapping an input).  Other arguments as for moe_finalize without a
- * residual.  The partial is read by every rank's phase 2.
+ * residual, and launched as moe_finalize is, under moe_finalize_plan(T, K,
+ * H, 0, ...); each element gets the same fp32 operations in the same order
+ * as the rank's partial inside moe_finalize_allreduce, so the two forms stay
+ * bit-identical.  The partial is read by every rank's phase 2.
  */
 moef_status moe_finalize_partial(const void *permuted_out, int64_t P,
                                  const int32_t *idx_map,
@@ -424,8 +427,8 @@ typedef struct {
  * moe_finalize_allreduce_plan -- the plan of the one-shot and phase-2 calls
  * (the two share it, which keeps their results bit-identical: lanes = R at
  * decode sizes; for even R >= 4 from 8 tokens on, groups of ranks, R / 2 or
- * 2 of them; 1 from 64 tokens on), or of phase 1 with R = 1 and
- * with_norm = 0.  Pure host computation: the plan depends on its arguments
+ * 2 of them; 1 from 64 tokens on).  with_norm = 0 plans the calls without
+ * a residual.  Pure host computation: the plan depends on its arguments
  * only, num_sms included, so every call with the same arguments gets the
  * same plan.
  * Returns MOEF_ERR_SHAPE when an RMSNorm row is too long for one cluster

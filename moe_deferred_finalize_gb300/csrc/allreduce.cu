@@ -10,16 +10,19 @@
 //   out = bf16(m);  residual_out = bf16(m + residual);
 //   norm_out = bf16(residual_out * rsqrt(mean(residual_out^2) + eps) * gamma)
 //
-// Three kernel templates serve three entry points:
+// The kernel templates here serve two entry points:
 //   * one-shot (moe_finalize_allreduce): every rank's rows are gathered in
 //     one launch, from local or peer-mapped memory;
-//   * phase 1 (moe_finalize_partial): one rank's p_r, stored in fp32;
 //   * phase 2 (moe_finalize_allreduce_reduce): the fp32 partials of all
 //     ranks summed, then the epilogue.
-// The one-shot and the two-phase forms run the same arithmetic in the same
-// order under the same launch plan, so their results are bit-identical.
+// Phase 1 (moe_finalize_partial, one rank's p_r stored in fp32) is the plain
+// finalize kernel's fp32-output build: the same fp32 operations on each
+// element in the same order as a rank's partial here.  The one-shot and the
+// two-phase forms therefore run the same arithmetic in the same order, and
+// phase 2 keeps the one-shot's launch plan, so their results are
+// bit-identical.
 //
-// Thread layout of the gathering kernels (one-shot, phase 1): a CTA's
+// Thread layout of the one-shot kernels: a CTA's
 // threads form `lanes` groups of `nvc` threads, and group g works for the
 // R / lanes consecutive ranks from g * R / lanes on.  In one pass thread
 // (g, j) obtains its ranks' partials of vector j of the CTA's slice one
@@ -63,7 +66,7 @@ constexpr int kArMaxThreads = 512;
 constexpr int kArMaxCluster = 16;
 constexpr int kMaxSlots = MOEF_MAX_RANKS * MOEF_MAX_K;
 
-// fp32 vectors of the partials: 8 values as two 16-byte accesses, or one.
+// fp32 vectors of the partials: 8 values as two 16-byte loads, or one.
 template <int VEC>
 struct F32Ops;
 
@@ -75,16 +78,11 @@ struct F32Ops<8> {
         f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
         f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
     }
-    static __device__ __forceinline__ void store(float *p, const float f[8]) {
-        reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
-        reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
-    }
 };
 
 template <>
 struct F32Ops<1> {
     static __device__ __forceinline__ void load(const float *p, float f[1]) { f[0] = __ldcs(p); }
-    static __device__ __forceinline__ void store(float *p, const float f[1]) { p[0] = f[0]; }
 };
 
 // Rank r's entry of a per-rank pointer array of the kernel parameters.  Each
@@ -133,17 +131,13 @@ __device__ __forceinline__ void rank_partial(const uint16_t *const *rows, const 
 }
 
 // The finishing thread's epilogue of one rank-summed vector `acc` at element
-// offset `at`: the fp32 partial (phase 1); or out, then with RMSNorm the
-// residual add, residual_out, the kept bf16 vector and its sum of squares.
+// offset `at`: out, then with RMSNorm the residual add, residual_out, the
+// kept bf16 vector and its sum of squares.
 template <int VEC, bool NORM>
 __device__ __forceinline__ void finish_vector(const ArParams &p, int64_t at, float (&acc)[VEC],
                                               const typename VecOps<VEC>::V &rs,
                                               typename VecOps<VEC>::V *keep, float &ss) {
     using Ops = VecOps<VEC>;
-    if (p.partial_out) {
-        F32Ops<VEC>::store(p.partial_out + at, acc);
-        return;
-    }
     if (p.out) Ops::store(p.out + at, Ops::from_f32(acc));
     if constexpr (NORM) {
         float f[VEC];
@@ -215,9 +209,8 @@ __device__ __forceinline__ void norm_tail(const ArParams &p, bool finisher, int 
     }
 }
 
-// One rank per group (lanes = R): the one-shot call (every rank's rows) and
-// phase 1 (one rank, fp32 partial out), and, with p.reduce, phase 2 of the
-// same plans over the ranks' fp32 partials, a thread per rank and vector
+// One rank per group (lanes = R): the one-shot call (every rank's rows),
+// and, with p.reduce, phase 2 of the same plans over the ranks' fp32 partials, a thread per rank and vector
 // keeping the partials' loads spread over the CTA.  Every group's partial of
 // a pass meets group 0 in shared memory.
 // PASSES: with RMSNorm, the number of passes over the slice (1, 2, 4 or 8),
@@ -228,9 +221,8 @@ __device__ __forceinline__ void norm_tail(const ArParams &p, bool finisher, int 
 // 128 registers) for smaller grids, whose time is a chain of memory
 // latencies: there the registers let every gathered load of a vector go out
 // before the first FMA, while 64 registers with RMSNorm spill and split them.
-// (Measured on GB300: building the phase-1/one-shot-only form of this
-// kernel, without the phase-2 branch, made the decode calls 0.1-0.35 us
-// slower.)
+// (Measured on GB300: building the one-shot-only form of this kernel,
+// without the phase-2 branch, made the decode calls 0.1-0.35 us slower.)
 // KC: K when fixed at compile time (top-8), else 0.
 template <int VEC, bool NORM, bool CLUSTER, int PASSES, int MINB, int KC>
 __global__ void __launch_bounds__(kArMaxThreads, MINB)

@@ -224,6 +224,7 @@ moef_status check_finalize_args(const void *permuted_out, int64_t P, const int32
     p->out = static_cast<uint16_t *>(out);
     p->residual_out = static_cast<uint16_t *>(residual_out);
     p->norm_out = static_cast<uint16_t *>(norm_out);
+    p->out_f32 = nullptr;
     p->routed_scale = routed_scale;
     p->eps = eps;
     p->wkind = static_cast<int>(wkind);
@@ -538,7 +539,7 @@ moef_status moe_finalize_allreduce_plan(int R, int T, int H, int with_norm, int 
             sl = nv;
             sp = ceil_div(nvec, sl);
             // two vectors a thread when one a thread would take more than one
-            // wave (phase 1, T = 256: 8.20 -> 8.04 us; T = 1024: 28.8 -> 28.1 us)
+            // wave (R = 1, T = 256: 8.20 -> 8.04 us; T = 1024: 28.8 -> 28.1 us)
             if (rows * sp > static_cast<int64_t>(num_sms) * (1024 / round_up(ln * nv, 32))) {
                 sl = 2 * nv;
                 sp = ceil_div(nvec, sl);
@@ -750,17 +751,30 @@ moef_status moe_finalize_partial(const void *permuted_out, int64_t P, const int3
     if (!partial) return MOEF_ERR_NULL;
     if (!aligned(partial, 4)) return MOEF_ERR_ALIGN;
     if (!aligned(partial, 16)) vec_ok = false;
-    moef::ArParams p = {};
-    p.x[0] = static_cast<const uint16_t *>(permuted_out);
-    p.idx[0] = idx_map;
-    p.weights[0] = weights;
-    p.shared[0] = static_cast<const uint16_t *>(shared_out);
-    p.partial_out = partial;
-    p.routed_scale = routed_scale;
-    p.wkind = static_cast<int>(wkind);
-    p.K = K;
-    p.reduce = 0;
-    return launch_ar(p, 1, T, H, false, vec_ok, stream);
+    // the plain finalize kernel, storing m unrounded: per element the same
+    // fp32 operations in the same order as a rank's partial in the one-shot
+    // kernel (and 0.15-0.6 us faster than that kernel's phase-1 form at
+    // T <= 64, the same at T = 256)
+    moef::FinalizeParams f = {};
+    f.x = static_cast<const uint16_t *>(permuted_out);
+    f.idx = idx_map;
+    f.weights = weights;
+    f.shared = static_cast<const uint16_t *>(shared_out);
+    f.out_f32 = partial;
+    f.routed_scale = routed_scale;
+    f.wkind = static_cast<int>(wkind);
+    f.T = T;
+    f.K = K;
+    f.H = H;
+    f.pdl = 1;
+    int sms = 0;
+    st = cuda_status(current_sms(&sms));
+    if (st != MOEF_OK) return st;
+    moef_plan plan;
+    st = moe_finalize_plan(T, K, H, 0, vec_ok ? 1 : 0, sms, 0, 0, &plan);
+    if (st != MOEF_OK) return st;
+    apply_plan(plan, &f);
+    return cuda_status(moef::launch_finalize(f, plan, sms, stream));
 }
 
 moef_status moe_finalize_allreduce_reduce(const float *const *partials, int R,

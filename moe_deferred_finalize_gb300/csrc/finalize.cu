@@ -58,8 +58,21 @@ namespace {
 constexpr int kMaxThreads = 256;
 constexpr int kMaxClusterCtas = 16;
 
+// fp32 vector store: 8 values as two 16-byte stores, or one value.
+template <int VEC>
+__device__ __forceinline__ void store_f32(float *q, const float (&f)[VEC]) {
+    if constexpr (VEC == 8) {
+        reinterpret_cast<float4 *>(q)[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4 *>(q)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    } else {
+        q[0] = f[0];
+    }
+}
+
 // KC: the slot count K when fixed at compile time, else 0 (K from p.K).
-template <int VPT, int VEC, bool NORM, bool CLUSTER, int KC>
+// F32: m is stored unrounded to p.out_f32 (fp32) instead of out (one
+// tensor-parallel rank's partial, without residual or RMSNorm).
+template <int VPT, int VEC, bool NORM, bool CLUSTER, int KC, bool F32>
 __global__ void __launch_bounds__(kMaxThreads)
 finalize_kernel(const __grid_constant__ FinalizeParams p) {
     using Ops = VecOps<VEC>;
@@ -163,7 +176,11 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
                 Ops::to_f32(sh, f);
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) acc[q] += f[q];
-                if (p.out) Ops::store(p.out + tok + e, Ops::from_f32(acc));
+                if constexpr (F32) {
+                    store_f32<VEC>(p.out_f32 + tok + e, acc);
+                } else if (p.out) {
+                    Ops::store(p.out + tok + e, Ops::from_f32(acc));
+                }
                 if (NORM) {
                     Ops::to_f32(rs, f);
 #pragma unroll
@@ -233,12 +250,12 @@ finalize_kernel(const __grid_constant__ FinalizeParams p) {
 
 constexpr int kFixedK = 8;
 
-template <int VPT, int VEC, bool NORM, bool CLUSTER>
+template <int VPT, int VEC, bool NORM, bool CLUSTER, bool F32 = false>
 cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, int num_sms,
                      cudaStream_t stream) {
     const int fixed_k = (p.K == kFixedK && plan.grid > num_sms) ? 1 : 0;
-    auto kern = fixed_k ? finalize_kernel<VPT, VEC, NORM, CLUSTER, kFixedK>
-                        : finalize_kernel<VPT, VEC, NORM, CLUSTER, 0>;
+    auto kern = fixed_k ? finalize_kernel<VPT, VEC, NORM, CLUSTER, kFixedK, F32>
+                        : finalize_kernel<VPT, VEC, NORM, CLUSTER, 0, F32>;
     cudaLaunchAttribute attr[2];
     unsigned num_attrs = 0;
     if (p.pdl) {
@@ -282,6 +299,10 @@ cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, int num_sms
 template <int VPT, int VEC>
 cudaError_t launch_v(const FinalizeParams &p, const moef_plan &plan, int num_sms,
                      cudaStream_t stream) {
+    if (p.out_f32) {
+        if (p.residual) return cudaErrorInvalidValue;
+        return launch_t<VPT, VEC, false, false, true>(p, plan, num_sms, stream);
+    }
     if (!p.residual) return launch_t<VPT, VEC, false, false>(p, plan, num_sms, stream);
     if (plan.cluster > 1) return launch_t<VPT, VEC, true, true>(p, plan, num_sms, stream);
     return launch_t<VPT, VEC, true, false>(p, plan, num_sms, stream);

@@ -21,6 +21,7 @@ struct FinalizeParams {
     uint16_t *out;              // bf16 [T, H] or null
     uint16_t *residual_out;     // bf16 [T, H] or null
     uint16_t *norm_out;         // bf16 [T, H] or null
+    float *out_f32;             // fp32 [T, H] or null: m unrounded, in place of out
     float routed_scale;
     float eps;
     int wkind;
@@ -38,7 +39,7 @@ cudaError_t launch_finalize(const FinalizeParams &p, const moef_plan &plan, int 
                             cudaStream_t stream);
 
 // Everything one launch of the all-reduce-fused finalize kernel needs
-// (one-shot, phase 1 or phase 2; allreduce.cu).
+// (one-shot or phase 2; allreduce.cu).
 struct ArParams {
     const uint16_t *x[MOEF_MAX_RANKS];          // each rank's permuted_out, bf16 [P_r, H]
     const int32_t *idx[MOEF_MAX_RANKS];         // each rank's [T, K] row map
@@ -50,13 +51,12 @@ struct ArParams {
     uint16_t *out;                              // bf16 [T, H] or null
     uint16_t *residual_out;                     // bf16 [T, H] or null
     uint16_t *norm_out;                         // bf16 [T, H] or null
-    float *partial_out;                         // phase 1: fp32 [T, H], else null
     float routed_scale;
     float eps;
     int wkind;
     int K, H;
     int nvec;                                   // vectors per row
-    int ranks;                                  // R: ranks summed (1 in phase 1)
+    int ranks;                                  // R: ranks summed
     int lanes;                                  // thread groups per CTA: R, or 1
     int nvc;                                    // threads per group = vectors per pass
     int splits;                                 // CTAs per token
