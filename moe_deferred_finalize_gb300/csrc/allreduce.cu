@@ -596,11 +596,12 @@ cudaError_t launch_ar_t(const ArParams &p, const moef_ar_plan &plan, int num_sms
     // to 16 such CTAs are resident at once
     const int64_t rows = plan.grid / plan.splits;
     const bool small = plan.grid <= num_sms && (plan.threads <= 256 || rows <= 7);
-    // phase 2 of a one-rank-per-group plan: in its rank groups over a small
-    // grid, else in the finishing threads alone, which load every rank's
-    // partial at once (R = 8, T = 8: 2.91 against 3.23 us; R = 3, T = 32:
-    // 3.20 against 4.28 us; R = 2, T = 48: 3.32 against 4.44 us)
-    if (plan.lanes == p.ranks && !(p.reduce && !small)) {
+    // phase 2 of a one-rank-per-group plan: in the finishing threads alone,
+    // which load every rank's partial at once (R = 8, T = 1: 2.55 against
+    // 2.69 us; T = 8: 2.91 against 3.23 us; R = 3, T = 32: 3.20 against 4.28
+    // us; R = 2, T = 48: 3.32 against 4.44 us), except over small grids with
+    // up to 3 ranks, where the rank groups measured 0.05 us faster
+    if (plan.lanes == p.ranks && !(p.reduce && (!small || p.ranks >= 4))) {
         // one rank per group: gathering, or phase 2 in rank groups.  Top-8
         // gathers over large grids take the build with K fixed (R = 8, T = 8:
         // 6.09 -> 5.74 us; R = 4, T = 32: 7.03 -> 6.41 us); the small-grid
