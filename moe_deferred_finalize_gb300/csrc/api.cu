@@ -92,10 +92,20 @@ const char *moef_status_string(moef_status s) {
 //    two vectors each fit it in one (T = 256: 7.2 vs 7.7 us).
 //  * with RMSNorm a row must be finished by one CTA or one cluster.  Rows
 //    start as slices of at most 256 vectors (one per thread of a 256-thread
-//    CTA, 4-CTA clusters at H = 7168), and the split is halved while the
-//    grid exceeds about 3.5 CTAs per SM (the best grids measured held
-//    384-512 CTAs); with no split one CTA takes a whole row (256 threads
-//    below 4 rows per SM or for rows of at most 512 vectors, then 128).
+//    CTA, 4-CTA clusters at H = 7168).  The aim is a grid of one wave,
+//    which held up to about 4.75 CTAs of 224 threads per SM, 4.25 of 256
+//    threads and 7.5 of 128 threads (a step past that cost a wave more:
+//    7.74 per SM fitted in 4-CTA clusters, not in 3-CTA ones).  So past
+//    that size the same slices go to 128-thread CTAs with two vectors a
+//    thread while those fit (H = 7168, T = 192 / 256: 8.52 / 9.68 -> 8.29 /
+//    9.24 us; H = 5120, T = 300: 9.03 -> 8.80 us), unless a whole row fits
+//    one CTA at two vectors a thread, which then wins without a cluster
+//    (H = 4096, T = 400: 8.18 against 9.11 us); otherwise the split is
+//    halved while the grid exceeds 4.25 CTAs per SM (H = 7168, T = 320:
+//    12.36 -> 10.75 us against the former 3.5 per SM, which also halved
+//    T = 144-176 too early: 7.56-8.30 -> 6.24-6.82 us); with no split one
+//    CTA takes a whole row (256 threads below 4 rows per SM or for rows of
+//    at most 512 vectors, then 128).
 //    7-CTA clusters at T = 512 were 1.5x slower than this.  At H = 2048 and
 //    4096, T = 2048, 256 threads beat 128 by 5.8 % and 2.9 %; at H = 5120
 //    and 7168, 128 threads win.
@@ -119,8 +129,22 @@ moef_status moe_finalize_plan(int T, int K, int H, int with_norm, int vec_ok, in
     } else if (with_norm) {
         const int row_fit = ceil_div(nvec, kMaxThreads * kMaxVpt);
         splits = ceil_div(nvec, kMaxThreads);
-        const int64_t cap = 7 * static_cast<int64_t>(num_sms) / 2;
-        while (splits > row_fit && splits > 1 && rows * splits > cap) splits = ceil_div(splits, 2);
+        // CTAs resident at once for a CTA size, in quarter CTAs per SM
+        const auto fits_one_wave = [&](int64_t ctas, int threads) {
+            const int64_t quarters = threads <= 128 ? 30 : threads <= 224 ? 19 : 17;
+            return 4 * ctas <= quarters * static_cast<int64_t>(num_sms);
+        };
+        const int sl0 = ceil_div(nvec, splits);
+        const int t0 = round_up(sl0 < kMaxThreads ? sl0 : kMaxThreads, 32);
+        if (splits > 1 && splits <= kMaxCluster && !fits_one_wave(rows * splits, t0)) {
+            if (t0 > 128 && nvec > 2 * kMaxThreads && fits_one_wave(rows * splits, 128)) {
+                threads_auto = 128;    // the same slices, two vectors a thread
+            } else {
+                while (splits > row_fit && splits > 1 &&
+                       !fits_one_wave(rows * splits, kMaxThreads))
+                    splits = ceil_div(splits, 2);
+            }
+        }
         if (splits < row_fit) splits = row_fit;
         if (splits > kMaxCluster) splits = kMaxCluster;
         // one CTA per row: 256 threads below 4 rows per SM, and for rows of at

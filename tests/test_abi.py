@@ -153,16 +153,24 @@ def test_plan_regimes(mf):
         (8, 7, 128, 128, 1, 1)
     p = mf.plan(16, 8, 7168, True)          # RMSNorm: 4-CTA clusters, one vector per thread
     assert (p["splits"], p["threads"], p["vpt"], p["cluster"], p["grid"]) == (4, 224, 1, 4, 64)
-    p = mf.plan(256, 8, 7168, True)
-    assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (2, 256, 2, 2)
-    p = mf.plan(512, 8, 7168, True)         # one CTA per row from ~3.5 CTAs per SM on
-    assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (1, 256, 4, 1)
-    p = mf.plan(192, 8, 7168, True)         # 4-CTA clusters would make 768 CTAs: halve
-    assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (2, 256, 2, 2)
-    p = mf.plan(384, 8, 7168, True)
-    assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == (1, 256, 4, 1)
-    p = mf.plan(128, 8, 7168, True)
-    assert (p["splits"], p["cluster"]) == (4, 4)
+    # one wave: up to 4.75 CTAs of 224 threads per SM (T <= 180 at 152 SMs),
+    # then the same slices on 128-thread CTAs, two vectors a thread, up to
+    # 7.5 per SM (T <= 285), then the split halved while above 4.25 per SM
+    # (T <= 323), then one CTA per row
+    for T, want in ((128, (4, 224, 1, 4)), (180, (4, 224, 1, 4)), (181, (4, 128, 2, 4)),
+                    (256, (4, 128, 2, 4)), (285, (4, 128, 2, 4)), (286, (2, 256, 2, 2)),
+                    (323, (2, 256, 2, 2)), (324, (1, 256, 4, 1)), (384, (1, 256, 4, 1)),
+                    (512, (1, 256, 4, 1))):
+        p = mf.plan(T, 8, 7168, True)
+        assert (p["splits"], p["threads"], p["vpt"], p["cluster"]) == want, (T, p)
+    # 256-thread slices (H = 4096) keep their size up to 4.25 CTAs per SM;
+    # past that a whole row goes to one CTA, two vectors a thread
+    assert mf.plan(323, 8, 4096, True)["threads"] == 256
+    p = mf.plan(324, 8, 4096, True)
+    assert (p["splits"], p["threads"], p["vpt"]) == (1, 256, 2)
+    p = mf.plan(380, 8, 5120, True)     # 3-CTA clusters of 128 threads up to 7.5 per SM
+    assert (p["splits"], p["threads"], p["vpt"]) == (3, 128, 2)
+    assert mf.plan(381, 8, 5120, True)["splits"] == 1
     p = mf.plan(128, 8, 7168, False)
     assert (p["splits"], p["threads"], p["vpt"], p["grid"]) == (7, 128, 1, 896)
     p = mf.plan(256, 8, 7168, False)        # 1792 CTAs: 64-thread CTAs fit one wave
