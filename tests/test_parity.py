@@ -61,6 +61,13 @@ CASES = [
     (2048, 8, 4096, "fp32", True),     # bandwidth regime, other hidden sizes
     (1500, 6, 5120, "bf16", True),
     (1200, 9, 8192, "packed", False),
+    # each RMSNorm plan of the mid-size batches at H = 7168 (one wave: 4-CTA
+    # clusters of 224 threads, then of 128 threads with two vectors each,
+    # then 2-CTA clusters), and 3-CTA clusters of 128 threads at H = 6144
+    (176, 8, 7168, "packed", True),
+    (256, 8, 7168, "fp32", True),
+    (300, 8, 7168, "bf16", True),
+    (360, 8, 6144, "fp32", True),
 ]
 
 
@@ -118,7 +125,8 @@ def test_launch_shapes_agree_without_norm(cuda_lib, orc, splits, threads):
 
 @pytest.mark.parametrize("norm,splits,threads", [
     (False, 1, 128), (False, 2, 128), (False, 4, 128), (False, 7, 128), (False, 1, 32),
-    (True, 1, 128), (True, 1, 256), (True, 2, 256), (True, 4, 224), (True, 16, 64)])
+    (True, 1, 128), (True, 1, 256), (True, 2, 256), (True, 4, 224), (True, 4, 128),
+    (True, 16, 64)])
 def test_fixed_k_and_any_k_builds_agree(cuda_lib, orc, norm, splits, threads):
     """With K = 8 a grid of more than one CTA per SM runs the build with K
     fixed at compile time, a smaller grid the any-K build.  The first tokens
