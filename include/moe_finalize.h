@@ -318,7 +318,11 @@ moef_status moe_finalize_unfused_noalloc(const void *permuted_out, int64_t P,
  *
  * The partials are summed in fp32, in the order of the rank array, so every
  * rank that passes the ranks in the same order obtains bit-identical
- * outputs, and the two forms below give bit-identical results.
+ * outputs, and the two forms below give bit-identical results.  (norm_out
+ * also depends on the order in which the sum of squares is added, which
+ * the launch plan fixes: it is bit-identical between calls whose buffers
+ * allow the same vector width, i.e. all 16-byte aligned with H % 8 == 0, or
+ * not; out and residual_out are bit-identical in every case.)
  *
  * Two forms, for two ways of ordering the ranks' work:
  *   one-shot  moe_finalize_allreduce: one launch reads every rank's rows
