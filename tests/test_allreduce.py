@@ -188,6 +188,28 @@ def test_partials_at_16_byte_aligned_addresses(cuda_lib):
     assert_same_bits(res, ref, "16-byte-aligned partials")
 
 
+def test_scalar_one_shot_against_vector_two_phase(cuda_lib, orc):
+    """A one-shot call whose outputs sit 2 bytes off a 16-byte boundary takes
+    the scalar path (its own plan); the two-phase form on aligned buffers
+    takes the 16-byte path.  out and residual_out are per-element the same
+    fp32 arithmetic and stay bit-identical; norm_out (whose sum of squares
+    each plan orders its own way) stays within tolerance of the oracle."""
+    g = W.tp_decode(2, 16)
+    rd = ranks_dev(g)
+    T, H = g.T, g.H
+    ref = oracle_ar(orc, g)
+    b, _ = two_phase(cuda_lib, g, rd, write_out=True)
+    bufs = {k: torch.empty(T * H + 1, dtype=torch.bfloat16, device="cuda")
+            for k in ("out", "residual_out", "norm_out")}
+    offs = {k: v[1:].view(T, H) for k, v in bufs.items()}
+    assert all(v.data_ptr() % 16 == 2 for v in offs.values())
+    a = one_shot(cuda_lib, g, rd, **offs)
+    for key in ("out", "residual_out"):
+        assert np.array_equal(bits_of(a[key]), bits_of(b[key])), key
+    compare(a, ref, "scalar one-shot: ")
+    compare(b, ref, "vector two-phase: ")
+
+
 def test_one_rank_is_the_plain_finalize(cuda_lib, orc):
     """R = 1: out and residual_out equal moe_finalize's bit for bit (same fp32
     operations in the same order); norm_out within tolerance of the oracle."""
