@@ -30,11 +30,13 @@
 // Two builds of every launch shape: one for the common top-8 routing, with
 // K fixed at compile time, and one for any K.  With K fixed the compiler
 // needs 40-56 registers instead of 64, so more CTAs fit an SM, which pays
-// once the grid exceeds one CTA per SM (about 1 % at T >= 256).  On grids of
-// at most one CTA per SM the time is a chain of memory latencies, and there
-// the any-K build, which issues all of a vector's K row loads before its
-// first FMA, is faster (T=1: 2.37 vs 2.68 us).  Both sum the K terms in the
-// same order, so their results are bit-identical.
+// on larger grids: with RMSNorm from one CTA per SM (T = 48: 3.98 vs 4.04
+// us; T = 96: 5.17 vs 5.53 us), without it from four (T = 96: 3.81 vs 3.87
+// us; T = 128: 4.26 vs 4.43 us).  On smaller grids the time is a chain of
+// memory latencies, and there the any-K build, which issues all of a
+// vector's K row loads before its first FMA, is faster (T = 1: 2.37 vs 2.68
+// us; without RMSNorm T = 32: 2.79 vs 3.10 us).  Both sum the K terms in
+// the same order, so their results are bit-identical.
 //
 // Launch order: the kernel is a programmatic dependent of the previous
 // kernel on the stream.  It touches global memory only after
@@ -253,7 +255,8 @@ constexpr int kFixedK = 8;
 template <int VPT, int VEC, bool NORM, bool CLUSTER, bool F32 = false>
 cudaError_t launch_t(const FinalizeParams &p, const moef_plan &plan, int num_sms,
                      cudaStream_t stream) {
-    const int fixed_k = (p.K == kFixedK && plan.grid > num_sms) ? 1 : 0;
+    const int64_t fixed_k_grid = static_cast<int64_t>(num_sms) * (NORM ? 1 : 4);
+    const int fixed_k = (p.K == kFixedK && plan.grid > fixed_k_grid) ? 1 : 0;
     auto kern = fixed_k ? finalize_kernel<VPT, VEC, NORM, CLUSTER, kFixedK, F32>
                         : finalize_kernel<VPT, VEC, NORM, CLUSTER, 0, F32>;
     cudaLaunchAttribute attr[2];

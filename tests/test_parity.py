@@ -128,15 +128,17 @@ def test_launch_shapes_agree_without_norm(cuda_lib, orc, splits, threads):
     (True, 1, 128), (True, 1, 256), (True, 2, 256), (True, 4, 224), (True, 4, 128),
     (True, 16, 64)])
 def test_fixed_k_and_any_k_builds_agree(cuda_lib, orc, norm, splits, threads):
-    """With K = 8 a grid of more than one CTA per SM runs the build with K
-    fixed at compile time, a smaller grid the any-K build.  The first tokens
-    of a large batch, finalized alone in the same launch shape, go through
-    the other build: every output must be bit-identical (same per-element
-    arithmetic and order), and the large batch must match the oracle."""
+    """With K = 8 a grid of more than one CTA per SM (with RMSNorm; four
+    without) runs the build with K fixed at compile time, a smaller grid the
+    any-K build.  The first tokens of a large batch, finalized alone in the
+    same launch shape, go through the other build: every output must be
+    bit-identical (same per-element arithmetic and order), and the large
+    batch must match the oracle."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    t_small = max(1, sms // splits)
-    t_large = sms + 8
-    assert t_small * splits <= sms < t_large * splits
+    limit = sms * (1 if norm else 4)
+    t_small = max(1, limit // splits)
+    t_large = limit // splits + 8
+    assert t_small * splits <= limit < t_large * splits
     wl = W.synth("builds", T=t_large, K=8, H=7168, E=256, tile=64, P=64 * 96,
                  weight_rule="sigmoid", routed_scale=2.5, with_norm=norm, seed=splits * 7 + norm,
                  require_all=False)
