@@ -88,9 +88,15 @@ pack_kernel(const int32_t *__restrict__ expert_ids, const float *__restrict__ we
 // key; only a lane that wins a second time before it has rescanned goes over
 // its keys again.
 //
-// Both leave the k-th selected logit on lane k; the weights are a softmax or
+// For E = 256 and K = 8 a faster selection runs first: one packed 32-bit
+// word per logit (the upper 24 bits of its key above its inverted id), a
+// sort of each lane's 8 words, and nine single-instruction warp maxima.  It
+// hands the token to the paths above when two of the nine largest words
+// could be out of order (equal upper key bits, different logits).
+//
+// All leave the k-th selected logit on lane k; the weights are a softmax or
 // a normalised sigmoid over the K kept logits (recovered exactly from their
-// keys), reduced across lanes 0..K-1.  Both select the same logits in the
+// keys), reduced across lanes 0..K-1.  All select the same logits in the
 // same order, so the outputs do not depend on which ran.
 constexpr int kRouteWarps = 4;
 
@@ -125,6 +131,20 @@ __device__ __forceinline__ void lane_best2(const uint32_t (&key)[EPL], uint32_t 
         } else if (kj > *b2) {
             *b2 = kj; *j2 = j;
         }
+    }
+}
+
+// Sorts 8 words into descending order in place (a 19-comparator network,
+// depth 6).
+__device__ __forceinline__ void sort8_desc(uint32_t (&w)[8]) {
+    constexpr int kPairs[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6},
+                                   {3, 7}, {0, 1}, {2, 3}, {4, 5}, {6, 7}, {2, 4}, {3, 5},
+                                   {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+    for (int c = 0; c < 19; ++c) {
+        const uint32_t a = w[kPairs[c][0]], b = w[kPairs[c][1]];
+        w[kPairs[c][0]] = max(a, b);
+        w[kPairs[c][1]] = min(a, b);
     }
 }
 
@@ -176,91 +196,137 @@ topk_route_kernel(const float *__restrict__ logits, int T, int E, int Kp, int ki
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     uint32_t kept_key = 0u, top_key = 0u;
     int kept_id = 0;
-
-    // Threshold: the K-th largest of the 32 lane maxima.  The K lanes holding
-    // the largest maxima hold K logits at or above it, so every one of the
-    // token's top K is at or above it too.
-    uint32_t lane_max = 0u;
+    bool selected = false;              // taken by the packed-word path
+    if constexpr (EPL == 8 && CONTIG && KT == 8) {
+        // E = 256, K = 8: each logit becomes one 32-bit word, the upper 24
+        // bits of its key above its inverted expert id, so that every word
+        // is unique and a larger word is a larger logit, or an equal one
+        // with a lower id.  Each lane sorts its 8 words; nine rounds of one
+        // warp maximum take the nine largest, the winning lane shifting its
+        // list.  The words order the logits exactly unless two share their
+        // upper 24 key bits with different values.  The winners' logits,
+        // read again, rule that out: adjacent winners with equal truncated
+        // keys must hold equal logits, and the 8th and 9th must differ in
+        // their truncated keys; otherwise the exact selection below runs.
+        uint32_t wd[8];
+        const uint32_t inv = 255u - static_cast<uint32_t>(lane * 8);
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) lane_max = max(lane_max, key[j]);
-    uint32_t theta = 0u;
-    {
-        // the lane number in the low 5 bits makes every lane's value unique,
-        // so one warp maximum names the winning lane
-        uint32_t mm = (lane_max & ~31u) | static_cast<uint32_t>(31 - lane);
-        for (int k = 0; k < K; ++k) {
-            theta = __reduce_max_sync(0xFFFFFFFFu, mm);
-            if (static_cast<int>(theta & 31u) == 31 - lane) mm = 0u;
-        }
-        theta &= ~31u;   // K lanes have maxima >= theta: still a lower bound
-    }
-    // theta > 0 (E >= K logits sit on at least K lanes), so empty slots
-    // (key 0) never count as candidates.
-    uint32_t cmask = 0u;
+        for (int j = 0; j < 8; ++j)
+            wd[j] = (key[j] & 0xFFFFFF00u) | (inv - static_cast<uint32_t>(j));
+        sort8_desc(wd);
+        uint32_t mine = 0u;             // lane r: the r-th largest word, r < 9
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) cmask |= (key[j] >= theta ? 1u : 0u) << j;
-    const unsigned cnt = __popc(cmask);
-    const unsigned C = __reduce_add_sync(0xFFFFFFFFu, cnt);
-    if (C <= 32u) {
-        const int w = threadIdx.x >> 5;
-        unsigned incl = cnt;            // inclusive prefix of the counts
+        for (int r = 0; r < 9; ++r) {
+            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, wd[0]);
+            if (lane == r) mine = m;
+            if (wd[0] == m) {
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        unsigned pos = incl - cnt;
-        // (key, inverted id) in one word: a larger word is a larger logit,
-        // or an equal logit with a lower id
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) {
-            if ((cmask >> j) & 1u) {
-                s_cand[w][pos] = (static_cast<uint64_t>(key[j]) << 32) |
-                                 (0xFFFFFFFFu - static_cast<uint32_t>(slot_id<EPL, CONTIG>(lane, j)));
-                ++pos;
+                for (int j = 0; j < 7; ++j) wd[j] = wd[j + 1];
+                wd[7] = 0u;
             }
         }
-        __syncwarp();
-        // lane i ranks candidate i against all of them
-        uint64_t mine = 0u;
-        unsigned rank = 32u;
-        if (lane < static_cast<int>(C)) {
-            mine = s_cand[w][lane];
-            rank = 0u;
+        const int id = 255 - static_cast<int>(mine & 255u);
+        float v = 0.f;
+        if (lane < 9) v = __ldg(z + id) + 0.f;
+        const uint32_t tr = mine >> 8;
+        const uint32_t tr_next = __shfl_down_sync(0xFFFFFFFFu, tr, 1);
+        const float v_next = __shfl_down_sync(0xFFFFFFFFu, v, 1);
+        const bool unsure = (lane < 7 && tr == tr_next && v != v_next) ||
+                            (lane == 7 && tr == tr_next);
+        if (!__any_sync(0xFFFFFFFFu, unsure)) {
+            selected = true;
+            kept_key = order_key(v);
+            kept_id = id;
+            top_key = __shfl_sync(0xFFFFFFFFu, kept_key, 0);
+        }
+    }
+    if (!selected) {
+
+        // Threshold: the K-th largest of the 32 lane maxima.  The K lanes holding
+        // the largest maxima hold K logits at or above it, so every one of the
+        // token's top K is at or above it too.
+        uint32_t lane_max = 0u;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) lane_max = max(lane_max, key[j]);
+        uint32_t theta = 0u;
+        {
+            // the lane number in the low 5 bits makes every lane's value unique,
+            // so one warp maximum names the winning lane
+            uint32_t mm = (lane_max & ~31u) | static_cast<uint32_t>(31 - lane);
+            for (int k = 0; k < K; ++k) {
+                theta = __reduce_max_sync(0xFFFFFFFFu, mm);
+                if (static_cast<int>(theta & 31u) == 31 - lane) mm = 0u;
+            }
+            theta &= ~31u;   // K lanes have maxima >= theta: still a lower bound
+        }
+        // theta > 0 (E >= K logits sit on at least K lanes), so empty slots
+        // (key 0) never count as candidates.
+        uint32_t cmask = 0u;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) cmask |= (key[j] >= theta ? 1u : 0u) << j;
+        const unsigned cnt = __popc(cmask);
+        const unsigned C = __reduce_add_sync(0xFFFFFFFFu, cnt);
+        if (C <= 32u) {
+            const int w = threadIdx.x >> 5;
+            unsigned incl = cnt;            // inclusive prefix of the counts
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            unsigned pos = incl - cnt;
+            // (key, inverted id) in one word: a larger word is a larger logit,
+            // or an equal logit with a lower id
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) {
+                if ((cmask >> j) & 1u) {
+                    s_cand[w][pos] = (static_cast<uint64_t>(key[j]) << 32) |
+                                     (0xFFFFFFFFu - static_cast<uint32_t>(slot_id<EPL, CONTIG>(lane, j)));
+                    ++pos;
+                }
+            }
+            __syncwarp();
+            // lane i ranks candidate i against all of them
+            uint64_t mine = 0u;
+            unsigned rank = 32u;
+            if (lane < static_cast<int>(C)) {
+                mine = s_cand[w][lane];
+                rank = 0u;
 #pragma unroll 4
-            for (unsigned j = 0; j < C; ++j) rank += s_cand[w][j] > mine ? 1u : 0u;
-        }
-        __syncwarp();
-        if (rank < static_cast<unsigned>(K)) s_cand[w][rank] = mine;
-        __syncwarp();
-        if (lane < K) {
-            const uint64_t kept = s_cand[w][lane];
-            kept_key = static_cast<uint32_t>(kept >> 32);
-            kept_id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kept));
-        }
-        top_key = static_cast<uint32_t>(s_cand[w][0] >> 32);
-    } else {                            // more than 32 candidates
-        uint32_t taken = 0u;            // slots this lane has given up
-        uint32_t b1, b2;
-        int j1, j2;
-        lane_best2(key, taken, &b1, &j1, &b2, &j2);
-        bool second_known = true;       // b2 is the lane's true second best
-        for (int k = 0; k < K; ++k) {
-            const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, b1);
-            const uint32_t wi = __reduce_min_sync(
-                0xFFFFFFFFu,
-                b1 == wk ? static_cast<uint32_t>(slot_id<EPL, CONTIG>(lane, j1)) : 0xFFFFFFFFu);
-            if (lane == k) { kept_key = wk; kept_id = static_cast<int>(wi); }
-            if (k == 0) top_key = wk;
-            if (slot_lane<EPL, CONTIG>(wi) == lane) {   // this lane's best was taken
-                taken |= 1u << j1;
-                if (second_known) {
-                    b1 = b2;
-                    j1 = j2;
-                    second_known = false;
-                } else {
-                    lane_best2(key, taken, &b1, &j1, &b2, &j2);
-                    second_known = true;
+                for (unsigned j = 0; j < C; ++j) rank += s_cand[w][j] > mine ? 1u : 0u;
+            }
+            __syncwarp();
+            if (rank < static_cast<unsigned>(K)) s_cand[w][rank] = mine;
+            __syncwarp();
+            if (lane < K) {
+                const uint64_t kept = s_cand[w][lane];
+                kept_key = static_cast<uint32_t>(kept >> 32);
+                kept_id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kept));
+            }
+            top_key = static_cast<uint32_t>(s_cand[w][0] >> 32);
+        } else {                            // more than 32 candidates
+            uint32_t taken = 0u;            // slots this lane has given up
+            uint32_t b1, b2;
+            int j1, j2;
+            lane_best2(key, taken, &b1, &j1, &b2, &j2);
+            bool second_known = true;       // b2 is the lane's true second best
+            for (int k = 0; k < K; ++k) {
+                const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, b1);
+                const uint32_t wi = __reduce_min_sync(
+                    0xFFFFFFFFu,
+                    b1 == wk ? static_cast<uint32_t>(slot_id<EPL, CONTIG>(lane, j1)) : 0xFFFFFFFFu);
+                if (lane == k) { kept_key = wk; kept_id = static_cast<int>(wi); }
+                if (k == 0) top_key = wk;
+                if (slot_lane<EPL, CONTIG>(wi) == lane) {   // this lane's best was taken
+                    taken |= 1u << j1;
+                    if (second_known) {
+                        b1 = b2;
+                        j1 = j2;
+                        second_known = false;
+                    } else {
+                        lane_best2(key, taken, &b1, &j1, &b2, &j2);
+                        second_known = true;
+                    }
                 }
             }
         }
