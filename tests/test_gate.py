@@ -119,6 +119,40 @@ def test_gate_then_finalize_with_packed_weights(cuda_lib, orc):
     compare(out, ref, "gate->finalize: ")
 
 
+def test_gate_packed_word_edge_cases(cuda_lib, orc):
+    """Top-8 of 256 first orders one 32-bit word per logit: the upper 24 bits
+    of its order key above its inverted id.  Tokens built to defeat that
+    ordering must still match the oracle bit for bit: the 12 largest logits
+    equal in their upper 24 key bits and different below, the 8th and 9th
+    differing only there, all 8 largest on one lane (its whole list taken),
+    and an exact tie inside the top 8 (which the words order by id)."""
+    rng = np.random.default_rng(2024)
+    T = 6
+    z = rng.standard_normal((T, 256)).astype(np.float32)
+    base = np.float32(3.0).view(np.uint32)
+    top = rng.choice(256, 12, replace=False)
+    low = rng.choice(256, 12, replace=False).astype(np.uint32)   # distinct low bits
+    z[0, top] = ((base & np.uint32(0xFFFFFF00)) | low).view(np.float32)
+    order = np.argsort(-z[1])
+    z[1, order[8]] = np.nextafter(z[1, order[7]], np.float32(np.inf))   # 9th above 8th by 1 ulp
+    z[2, 40:48] = 10.0 + np.arange(8, dtype=np.float32)           # lane 5 holds the top 8
+    z[3, [3, 200]] = 7.0                                          # an exact tie, ranks 1-2
+    z[4, [9, 17, 250]] = -0.0                                     # signed zeros among the rest
+    z[4, 100:108] = 2.0 + np.arange(8, dtype=np.float32)
+    z[5, :] = np.round(z[5, :] * 4) / 4                          # many ties
+    for kind in ("softmax", "sigmoid"):
+        res = cuda_lib.topk_route(torch.from_numpy(z).cuda(), 8, kind, want_packed=True)
+        torch.cuda.synchronize()
+        rid, rw = orc.topk_route(z, 8, kind)
+        ids = res["expert_ids"].cpu().numpy()
+        w = res["weights"].cpu().numpy()
+        assert np.array_equal(ids, rid), kind
+        assert np.allclose(w, rw, rtol=2e-6, atol=1e-9)
+        assert np.array_equal(res["packed"].cpu().numpy(), orc.pack_topk_ids(ids, w))
+    assert list(rid[2]) == list(range(47, 39, -1))
+    assert list(rid[3][:2]) == [3, 200]
+
+
 @pytest.mark.parametrize("n_top", [31, 32, 33, 40])
 def test_gate_candidate_count_boundary(cuda_lib, orc, n_top):
     """n_top equal largest logits spread over the lanes: with 32 or fewer the
