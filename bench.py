@@ -535,6 +535,23 @@ def allreduce_bytes(R, T, K, H, wbytes=4):
     return R * (T * K * H * 2 + T * H * 2 + T * K * (4 + wbytes)) + 3 * T * H * 2 + H * 2
 
 
+def allreduce_copies(R, T, K, H):
+    """Buffer copies the all-reduce entry rotates over: (C, Cr, bytes).  C
+    copies of every rank's operands for the one-shot; Cr copies of one
+    rank's operands, the R partials, residual and outputs for phase 1,
+    phase 2 and the plain finalize, as many as the smaller of phase 1's and
+    phase 2's working sets needs to exceed twice the L2 (capped at 4096).
+    bytes: the one-shot's, phase 1's and phase 2's algorithmic bytes."""
+    nbytes = allreduce_bytes(R, T, K, H)
+    p1_bytes = T * K * H * 2 + T * H * 2 + T * K * 8 + T * H * 4
+    p2_bytes = R * T * H * 4 + 3 * T * H * 2 + H * 2
+
+    def n_copies(b):
+        return int(min(max(2, np.ceil(2 * L2_BYTES / b)), 4096))
+
+    return n_copies(nbytes), n_copies(min(p1_bytes, p2_bytes)), (nbytes, p1_bytes, p2_bytes)
+
+
 def allreduce_latency(mf, device, R, T, peak, calls=1000):
     """µs per call of the all-reduce-fused finalize at decode size T over R
     ranks' buffer sets on this one GPU (CUDA-graph replay; every call on
@@ -555,14 +572,7 @@ def allreduce_latency(mf, device, R, T, peak, calls=1000):
     smallest of their working sets needs."""
     g = W.tp_decode(R, T)
     K, H = g.K, g.H
-    nbytes = allreduce_bytes(R, T, K, H)
-    p1_bytes = T * K * H * 2 + T * H * 2 + T * K * 8 + T * H * 4
-    p2_bytes = R * T * H * 4 + 3 * T * H * 2 + H * 2
-
-    def n_copies(b):
-        return int(min(max(2, np.ceil(2 * L2_BYTES / b)), 4096))
-
-    C, Cr = n_copies(nbytes), n_copies(min(p1_bytes, p2_bytes))
+    C, Cr, (nbytes, _, p2_bytes) = allreduce_copies(R, T, K, H)
 
     def rep(a, n):   # n copies at distinct addresses
         t = host_tensor(np.ascontiguousarray(a)).to(device)

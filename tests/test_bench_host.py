@@ -101,6 +101,22 @@ def test_allreduce_bytes():
     assert bench.allreduce_bytes(1, T, K, H) == bench.algorithmic_bytes(T, K, H, 4, True, False)
 
 
+def test_allreduce_rotation_exceeds_l2_for_every_timed_call():
+    """Each call the all-reduce entry times (one-shot; phase 1, phase 2 and
+    the plain finalize of one rank) rotates over copies that together hold
+    at least twice the L2, so none of them is timed from L2, unless the
+    copy count is at its cap."""
+    for R in (1, 2, 4, 8):
+        for T in (1, 16, 256, 1024):
+            C, Cr, (one, p1, p2) = bench.allreduce_copies(R, T, 8, 7168)
+            assert C == 4096 or C * one >= 2 * bench.L2_BYTES, (R, T)
+            for b in (p1, p2):
+                assert Cr == 4096 or Cr * b >= 2 * bench.L2_BYTES, (R, T, b)
+            # the one-rank calls touch fewer bytes, so they need at least as
+            # many copies as the one-shot
+            assert Cr >= C
+
+
 def test_per_config_summary_puts_the_oracle_beside_each_workload():
     decode = {k: {"us_per_call_graph": 2.0, "GBps_graph": 100.0, "frac": 0.01,
                   "us_bytes_at_peak": 0.1, "floor_us_dependent_launch": 1.7}
